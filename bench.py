@@ -1,0 +1,401 @@
+"""Benchmark of fused MSA decode (indexer -> top-16 select -> sparse attention) on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one msa_decode call over the whole batch of the workload (every row of the hot
+path: block scores of the full context, selection, attention, split merge), inputs
+resident in HBM.  Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own
+replica of the workload on its own GPU (weak scaling, no collective on the data path);
+the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MSA decode queries/s and achieved HBM GB/s (vs ~8 TB/s) at 128K ctx, 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20       # > 2x the 129 MB L2
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def replica_workload(name: str, rank: int):
+    """Rank r decodes its own replica of the named workload: same shapes, its own seed."""
+    from workloads import synthetic as syn
+    w0 = syn.WORKLOADS[name]
+    return syn.Workload(**{**w0.__dict__, "seed": w0.seed + 7919 * rank})
+
+
+def reduce_max(values, world_size: int, device=None):
+    """Element-wise max of a list of floats over all ranks (the job's time is its slowest rank)."""
+    if world_size <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of a workload: the first few sequences, all their
+    query tokens (the last 64 for prefill), caches quantised once before any timing."""
+
+    def __init__(self, workload_name: str, n_seqs: int, rank_seed_offset: int = 0):
+        from oracle import cache as OC
+        from workloads import synthetic as syn
+
+        w = syn.WORKLOADS[workload_name]
+        self.w = syn.Workload(**{**w.__dict__, "seed": w.seed + rank_seed_offset})
+        self.seqs = list(range(min(n_seqs, self.w.batch)))
+        _, self.table, self.lens = syn.layout(self.w)
+        self.cache, _, _, _ = OC.build_cache(self.w, self.lens, self.seqs, threads=os.cpu_count() or 1)
+        self.q, self.qi = OC.encode_queries(self.w, self.seqs)
+        T = self.w.q_len
+        self.tokens = list(range(T)) if T <= 64 else list(range(T - 64, T))
+
+    def run_one(self, b: int) -> int:
+        import numpy as np
+        from oracle import msa as OM
+
+        w, T = self.w, self.w.q_len
+        s = OM.block_scores(self.qi, self.cache[4], self.cache[5], self.table, self.lens, tokens=self.tokens,
+                            sequences=[b])
+        sel = np.full((w.batch, T, 4, 16), -1, np.int32)
+        for t in self.tokens:
+            for g in range(4):
+                sel[b, t, g] = OM.select_row(s[b, t, g], int(self.lens[b]) - T + t)
+        OM.sparse_attention(self.q, *self.cache[:4], self.table, self.lens, sel, w.heads_per_group,
+                            tokens=self.tokens, sequences=[b])
+        return len(self.tokens)
+
+    def timed(self, budget_s: float):
+        """Runs whole sequences of the sample (cycling) until budget_s; (queries/s, info)."""
+        t_total, rows, done = 0.0, 0, []
+        k = 0
+        while t_total < budget_s or not done:
+            b = self.seqs[k % len(self.seqs)]
+            t0 = time.perf_counter()
+            rows += self.run_one(b)
+            t_total += time.perf_counter() - t0
+            done.append(b)
+            k += 1
+        return rows / t_total, {"sequences": done, "query_rows": rows, "seconds": round(t_total, 3)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.barrier()
+            dist.destroy_process_group()
+            return
+    from workloads import synthetic as syn
+    w = syn.WORKLOADS[args.workload]
+    sample = OracleSample(args.workload, n_seqs=4)
+    per_step = max(0.5, args.ref_budget / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        sample.timed(per_step)
+    vals, info = [], None
+    for _ in range(args.steps):
+        v, info = sample.timed(per_step)
+        vals.append(v)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.batch * w.q_len / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "heads": w.num_heads,
+                       "kv_groups": 4, "head_dim": 128, "top_k": 16, "block": 128},
+            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"float64 numpy oracle (BLAS threads) on whole sequences of the workload "
+                                       f"(prebuilt cache), ~{per_step:.1f} s per step; last step {info}"},
+            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import block_sparse_attention_indexer_gb300 as msa
+    from oracle import msa as OM  # byte accounting of the oracle (host arithmetic, not the GPU path)
+    from workloads import device
+    from workloads import synthetic as syn
+
+    w0 = syn.WORKLOADS[args.workload]
+    w = replica_workload(args.workload, rank)      # weak scaling: one replica per rank
+    t_setup = time.perf_counter()
+    dw = device.upload(w)
+    setup_s = time.perf_counter() - t_setup
+    B, T, H = w.batch, w.q_len, w.num_heads
+    dev = torch.device("cuda", local)
+    out = torch.zeros(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros(B, T, H, dtype=torch.float32, device=dev)
+    sel = torch.zeros(B, T, 4, 16, dtype=torch.int32, device=dev)
+    wsp = msa.alloc_workspace(msa.MSA_OP_DECODE, dw.cfg, dw.batch, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, lse, sel, wsp, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_error(wsp) == 0
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    # ---- stage timing (same stream, same arguments) for the roofline of each kernel
+    scores = torch.empty(B, T, 4, dw.batch.max_blocks, dtype=torch.float32, device=dev)
+    ws_idx = msa.alloc_workspace(msa.MSA_OP_INDEXER_SCORES, dw.cfg, dw.batch, device=dev)
+    ws_att = msa.alloc_workspace(msa.MSA_OP_SPARSE_ATTN, dw.cfg, dw.batch, device=dev)
+
+    def timed(fn, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    idx_ms = timed(lambda: msa.msa_indexer_scores(dw.cfg, dw.cache, dw.batch, dw.qi, scores, ws_idx, stream),
+                   args.steps)
+    sel_ms = timed(lambda: msa.msa_select_blocks(dw.cfg, dw.batch, scores, sel, stream), args.steps)
+    att_ms = timed(lambda: msa.msa_sparse_attn_decode(dw.cfg, dw.cache, dw.batch, dw.q, sel, out, lse, ws_att,
+                                                      stream), args.steps)
+    clk = clocks.stop()
+
+    # ---- end to end through the public API with host buffers (pinned), every step:
+    # H2D of the step's queries, index queries, block table and lengths; D2H of the output
+    h_q = dw.q.cpu().pin_memory()
+    h_qi = dw.qi.cpu().pin_memory()
+    h_table = dw.batch.block_table.cpu().pin_memory()
+    h_lens = dw.batch.seq_lens.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_qi = torch.empty_like(dw.q), torch.empty_like(dw.qi)
+    d_table, d_lens = torch.empty_like(dw.batch.block_table), torch.empty_like(dw.batch.seq_lens)
+    e_batch = msa.Batch(d_table, d_lens, T)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qi, h_table, h_lens))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_qi.copy_(h_qi, non_blocking=True)
+        d_table.copy_(h_table, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        msa.msa_decode(dw.cfg, dw.cache, e_batch, d_q, d_qi, out, lse, None, wsp, stream)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_times = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        stream.synchronize()
+        e2e_times.append(time.perf_counter() - t0)
+    assert msa.msa_read_device_error(wsp) == 0
+
+    # ---- aggregate over ranks (max time)
+    ms_step = statistics.mean(step_ms)
+    e2e_s = statistics.mean(e2e_times)
+    ms_step, e2e_s, idx_ms, att_ms = reduce_max([ms_step, e2e_s, idx_ms, att_ms], ws, dev)
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    sel_h = sel.cpu().numpy()
+    idx_bytes, kv_bytes = OM.decode_step_bytes(dw.lens, sel_h)
+    queries = B * T
+    value = ws * queries / (ms_step / 1e3)
+    idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
+    att_gbs = kv_bytes / (att_ms / 1e3) / 1e9
+    step_gbs = (idx_bytes + kv_bytes) / (ms_step / 1e3) / 1e9
+    splits = 1
+    rows = B * T * 4
+    while splits < 16 and splits < -(-1024 // rows):
+        splits <<= 1
+    launches_per_step = 3 + (1 if splits > 1 else 0)
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                tj = json.load(f)
+            traffic = tj.get(w.name, {}).get("indexer_kernel_bytes_per_launch")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 mma (exact nvfp4/fp8 products), f32 acc", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "q_len": T, "heads": H, "kv_groups": 4, "head_dim": 128,
+                   "index_dim": 128, "top_k": 16, "block": 128, "mean_ctx": float(np.mean(dw.lens)),
+                   "tokens_in_cache": int(np.sum(dw.lens)), "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": f"replicas x{ws}"},
+        "achieved_hbm_gbs": step_gbs,
+        "step_roofline": {"bound": "hbm", "algorithmic_bytes": idx_bytes + kv_bytes, "achieved": step_gbs,
+                          "peak": peak, "unit": "GB/s", "frac": step_gbs / peak, "peak_kind": peak_kind,
+                          "frac_of_8tbs": step_gbs / 8000.0},
+        "roofline": {"bound": "hbm", "kernel": "indexer_kernel", "achieved": idx_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": idx_gbs / peak, "traffic": traffic, "algorithmic_bytes": idx_bytes,
+                     "peak_kind": f"{peak_kind} (burst copy)"},
+        "stages_ms": {"indexer": idx_ms, "select": sel_ms, "attention": att_ms,
+                      "attention_gbs": att_gbs, "attention_bytes": kv_bytes},
+        "e2e": {"value": ws * queries / e2e_s, "unit": "queries/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "setup_s": round(setup_s, 1),
+        "wall_s_timed_region": wall,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(w0.name, n_seqs=4)
+        v, info = sample.timed(args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"float64 numpy oracle (BLAS threads) on whole sequences of the same "
+                                          f"workload, cache prebuilt: {info}"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="ragged64_128k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

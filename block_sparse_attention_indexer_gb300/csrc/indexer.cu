@@ -1,0 +1,325 @@
+// Stage 1 of MSA decode: indexer score + block max-pool.
+//
+// "Ein leichtgewichtiger Indexer bewertet jeden Schlüssel im Kontext mit einer
+// Index-Abfrage pro GQA-Gruppe gegen einen einzigen gemeinsamen Index-Schlüssel-Kopf und
+// poolt diese Bewertungen dann per Max-Pooling zu einer Bewertung pro Block" -- restated:
+// every cached key j is scored against one index query per (query token, KV group), and
+// the scores of a 128-token block are reduced with max over the keys visible to the query
+// ("vLLM liefert Day-0-Unterstützung für MiniMax-M3.1-Flash", §MSA-Grundlagen; masks from
+// "MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署", §MSA 机制细节).
+//
+// Design (GB300): the path is HBM-bound (72 bytes of NVFP4 index key per token, read
+// once per step), so the kernel is a persistent streaming scan:
+//   * one CTA per SM, 8 independent warps; the flattened list of (sequence, page, query
+//     chunk) units is split into equal contiguous ranges, one per warp (balanced to one
+//     unit whatever the ragged lengths);
+//   * each warp streams its pages with a private 2-stage ring of 9 KB shared-memory
+//     buffers filled by bulk async copies (cp.async.bulk + mbarrier), so ~72 KB per SM is
+//     always in flight;
+//   * scores run on the tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate) with keys
+//     as M (16 per tile) and query rows (token, group) as N: one packed E2M1 byte becomes
+//     one f16x2 A register (cvt.rn.f16x2.e2m1x2), the block scale multiplies it in f16
+//     (E2M1 x E4M3 products are exact in f16), and the FP8 index query widens exactly to
+//     f16, so every product is exact and only the f32 accumulation rounds -- the exact-score
+//     idea of the Rubin section of the M3.1 post, instead of re-rounding keys to FP8;
+//   * the contraction order over the 128 dims is permuted so that each lane reads 16
+//     contiguous bytes per key row (the dot product is order-free; the queries use the same
+//     permutation);
+//   * the max-pool is a register max over the 8 key tiles of a page followed by a 3-step
+//     shuffle reduction; per-token scores never leave registers.
+#include <cuda_fp16.h>
+
+#include "msa_device.cuh"
+#include "msa_kernels.h"
+
+namespace msa {
+
+constexpr int kIdxWarps = 8;
+constexpr int kIdxStages = 2;
+constexpr int kStageBytes = kPageData + kPageScale;  // 9216
+
+__device__ __forceinline__ int find_seq(const int32_t* prefix, int batch, int64_t u) {
+  // largest b with prefix[b] <= u (prefix is non-decreasing, prefix[batch] > u)
+  int lo = 0, hi = batch;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const IndexerArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kIdxWarps * kIdxStages * kStageBytes);
+  int32_t* prefix = reinterpret_cast<int32_t*>(bars + kIdxWarps * kIdxStages);
+  __shared__ int32_t warp_tot[kIdxWarps];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int T = a.q_len, G = a.groups, TC = a.chunk_tokens;
+  const int nchunks = (T + TC - 1) / TC;
+  const int64_t cap = static_cast<int64_t>(a.max_blocks) * kBlock;
+
+  // ---- units per sequence and their exclusive prefix (block-wide scan)
+  {
+    const int per = (a.batch + blockDim.x - 1) / blockDim.x;
+    const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) {
+      const int L = a.seq_lens[b];
+      const bool ok = (L >= T) && (L <= cap);
+      if (L != 0 && !ok && blockIdx.x == 0) flag_error(a.err, MSA_DEVERR_BAD_SEQLEN);
+      local += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + incl - local;
+    for (int b = lo; b < hi; ++b) {
+      prefix[b] = run;
+      const int L = a.seq_lens[b];
+      const bool ok = (L >= T) && (L <= cap);
+      run += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
+    }
+    if (tid == blockDim.x - 1) {
+      int tot = 0;
+      for (int w = 0; w < kIdxWarps; ++w) tot += warp_tot[w];
+      prefix[a.batch] = tot;
+    }
+  }
+  if (lane == 0)
+    for (int s = 0; s < kIdxStages; ++s) mbar_init(&bars[warp * kIdxStages + s], 1);
+  fence_mbar_init();
+  __syncthreads();
+
+  const int64_t total = prefix[a.batch];
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kIdxWarps;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kIdxWarps + warp;
+  const int64_t u0 = total * gw / nwarps, u1 = total * (gw + 1) / nwarps;
+
+  uint8_t* my_stages = stages + warp * kIdxStages * kStageBytes;
+  uint64_t* my_bars = bars + warp * kIdxStages;
+
+  // ---- issue side: page-granular cursor running ahead of the consumer
+  int64_t ucur_issue = u0;
+  auto issue_next = [&](int stage) {
+    // all lanes evaluate (uniform); lane 0 issues
+    const int b = find_seq(prefix, a.batch, ucur_issue);
+    const int64_t local = ucur_issue - prefix[b];
+    const int n = static_cast<int>(local / nchunks);
+    const int64_t end = prefix[b] + static_cast<int64_t>(n + 1) * nchunks;
+    ucur_issue = end < u1 ? end : u1;
+    const int page = a.block_table[static_cast<int64_t>(b) * a.max_blocks + n];
+    if (lane == 0) {
+      uint64_t* bar = &my_bars[stage];
+      if (page >= 0 && page < a.num_pages) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        uint8_t* dst = my_stages + stage * kStageBytes;
+        bulk_g2s(dst, a.idx_data + static_cast<int64_t>(page) * kPageData, kPageData, bar);
+        bulk_g2s(dst + kPageData, a.idx_scale + static_cast<int64_t>(page) * kPageScale, kPageScale, bar);
+      } else {
+        flag_error(a.err, MSA_DEVERR_BAD_PAGE);
+        mbar_arrive(bar);
+      }
+    }
+  };
+
+  int issued = 0;
+  for (int s = 0; s < kIdxStages && ucur_issue < u1; ++s, ++issued) issue_next(s);
+
+  // ---- consumer state
+  uint32_t bq[NT][8][2];  // B fragments (index queries), one chunk of one sequence
+  int cur_b = -1, cur_c = -1;
+  int64_t ucur = u0;
+  int consumed = 0;
+  bool timed_out = false;
+
+  while (ucur < u1) {
+    const int b = find_seq(prefix, a.batch, ucur);
+    const int64_t local = ucur - prefix[b];
+    const int n = static_cast<int>(local / nchunks);
+    const int c_lo = static_cast<int>(local - static_cast<int64_t>(n) * nchunks);
+    const int64_t end = prefix[b] + static_cast<int64_t>(n + 1) * nchunks;
+    const int64_t uend = end < u1 ? end : u1;
+    const int c_hi = c_lo + static_cast<int>(uend - ucur);
+    const int stage = consumed % kIdxStages;
+    const uint32_t parity = (consumed / kIdxStages) & 1;
+    const int page = a.block_table[static_cast<int64_t>(b) * a.max_blocks + n];
+    const bool page_ok = page >= 0 && page < a.num_pages;
+    const int L = a.seq_lens[b];
+
+    if (!mbar_wait_warp(&my_bars[stage], parity)) {
+      timed_out = true;
+      break;
+    }
+    const uint8_t* st = my_stages + stage * kStageBytes;
+
+    for (int c = c_lo; c < c_hi; ++c) {
+      const int t0 = c * TC;
+      const int tc = min(TC, T - t0);
+      const int rows = tc * G;
+      const int pos_min = L - T + t0, pos_max = pos_min + tc - 1;
+      float mx[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = -INFINITY;
+
+      if (page_ok && n * kBlock <= pos_max) {
+        if (b != cur_b || c != cur_c) {
+          cur_b = b;
+          cur_c = c;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int r = nt * 8 + g;
+            if (r < rows) {
+              const int tq = t0 + r / G, gq = r % G;
+              const uint4* src = reinterpret_cast<const uint4*>(
+                  a.index_q + ((static_cast<int64_t>(b) * T + tq) * G + gq) * kDim + 32 * t4);
+              const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+              const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+              for (int s = 0; s < 8; ++s) {
+                bq[nt][s][0] = e4m3x2_to_f16x2(w[s]);
+                bq[nt][s][1] = e4m3x2_to_f16x2(w[s] >> 16);
+              }
+            } else {
+#pragma unroll
+              for (int s = 0; s < 8; ++s) bq[nt][s][0] = bq[nt][s][1] = 0u;
+            }
+          }
+        }
+        // per column: the query position it belongs to (for the causal / tail mask)
+        int posc[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = nt * 8 + 2 * t4 + e;
+            posc[nt][e] = col < rows ? (L - T + t0 + col / G) : -1;
+          }
+        const bool need_mask = (n + 1) * kBlock - 1 > pos_min;
+
+#pragma unroll 2
+        for (int mt = 0; mt < 8; ++mt) {
+          const int r0 = mt * 16 + g, r1 = r0 + 8;
+          const uint4 d0 = lds128(st + r0 * kRowBytes + 16 * t4);
+          const uint4 d1 = lds128(st + r1 * kRowBytes + 16 * t4);
+          const uint32_t s0 = lds16(st + kPageData + r0 * kRowScales + 2 * t4);
+          const uint32_t s1 = lds16(st + kPageData + r1 * kRowScales + 2 * t4);
+          const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
+          const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
+          const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
+          const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
+          float acc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+            e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
+            e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
+            const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
+            x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
+            y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_f16_16816(acc[nt], x0, y0, x1, y1, bq[nt][2 * w][0], bq[nt][2 * w][1]);
+              mma_f16_16816(acc[nt], x2, y2, x3, y3, bq[nt][2 * w + 1][0], bq[nt][2 * w + 1][1]);
+            }
+          }
+          if (need_mask) {
+            const int j0 = n * kBlock + r0, j1 = j0 + 8;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              if (j0 > posc[nt][0]) acc[nt][0] = -INFINITY;
+              if (j0 > posc[nt][1]) acc[nt][1] = -INFINITY;
+              if (j1 > posc[nt][0]) acc[nt][2] = -INFINITY;
+              if (j1 > posc[nt][1]) acc[nt][3] = -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mx[nt][0] = fmaxf(mx[nt][0], fmaxf(acc[nt][0], acc[nt][2]));
+            mx[nt][1] = fmaxf(mx[nt][1], fmaxf(acc[nt][1], acc[nt][3]));
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float v = mx[nt][e];
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+            mx[nt][e] = v;
+          }
+      }
+      if (g == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = nt * 8 + 2 * t4 + e;
+            if (col < rows) {
+              const int tq = t0 + col / G, gq = col % G;
+              a.block_scores[((static_cast<int64_t>(b) * T + tq) * G + gq) * a.max_blocks + n] = mx[nt][e];
+            }
+          }
+      }
+    }
+    __syncwarp();
+    ++consumed;
+    ucur = uend;
+    if (ucur_issue < u1) {
+      issue_next(issued % kIdxStages);
+      ++issued;
+    }
+  }
+
+  if (timed_out) {
+    if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
+    // drain this warp's copies still in flight (bounded) before leaving
+    for (int k = consumed; k < issued; ++k) mbar_wait(&my_bars[k % kIdxStages], (k / kIdxStages) & 1);
+  }
+
+  // ---- -inf for blocks past each sequence's end (and whole rows of skipped sequences)
+  const int64_t nrows = static_cast<int64_t>(a.batch) * T * G;
+  for (int64_t row = gw; row < nrows; row += nwarps) {
+    const int b = static_cast<int>(row / (static_cast<int64_t>(T) * G));
+    const int nb = (prefix[b + 1] - prefix[b]) / nchunks;
+    float* dst = a.block_scores + row * a.max_blocks;
+    for (int n = nb + lane; n < a.max_blocks; n += 32) dst[n] = -INFINITY;
+  }
+}
+
+template <int NT>
+static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(kIdxWarps) * kIdxStages * kStageBytes +
+                      kIdxWarps * kIdxStages * sizeof(uint64_t) + (a.batch + 1) * sizeof(int32_t);
+  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  indexer_kernel<NT><<<num_sms, kIdxWarps * 32, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+  const int rows = a.chunk_tokens * a.groups;
+  switch ((rows + 7) / 8) {
+    case 1: return launch_nt<1>(a, num_sms, s);
+    case 2: return launch_nt<2>(a, num_sms, s);
+    case 3: return launch_nt<3>(a, num_sms, s);
+    default: return launch_nt<4>(a, num_sms, s);
+  }
+}
+
+}  // namespace msa

@@ -1,0 +1,79 @@
+// Kernel argument blocks and launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Host-only declarations; every pointer is device memory.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msa {
+
+struct IndexerArgs {
+  const uint8_t* idx_data;     // [P][128][64]
+  const uint8_t* idx_scale;    // [P][128][8]
+  int64_t num_pages;
+  const int32_t* block_table;  // [B][max_blocks]
+  const int32_t* seq_lens;     // [B]
+  int32_t batch, max_blocks, q_len, groups;
+  int32_t chunk_tokens;        // query tokens per work chunk (rows = chunk_tokens * groups <= 32)
+  const uint8_t* index_q;      // [B][T][G][128] E4M3
+  float* block_scores;         // [B][T][G][max_blocks]
+  uint32_t* err;
+};
+
+struct SelectArgs {
+  const float* block_scores;   // [B][T][G][max_blocks]
+  const int32_t* seq_lens;
+  int32_t batch, max_blocks, q_len, groups;
+  int32_t* selection;          // [B][T][G][16]
+};
+
+struct AttnArgs {
+  const uint8_t* k_data;       // [P][G][128][64]
+  const uint8_t* k_scale;      // [P][G][128][8]
+  const uint8_t* v_data;
+  const uint8_t* v_scale;
+  int64_t num_pages;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t batch, max_blocks, q_len, groups, heads_per_group;
+  const uint8_t* q;            // [B][T][H][128] E4M3
+  const int32_t* selection;    // [B][T][G][16]
+  uint16_t* out;               // [B][T][H][128] bf16
+  float* lse;                  // [B][T][H] or null
+  float* partial;              // [B][T][H][splits][130] when splits > 1
+  int32_t splits;
+  float scale_log2;            // softmax_scale * log2(e)
+  uint32_t* err;
+};
+
+struct QuantArgs {
+  const float* x;
+  int64_t n_tokens;
+  int32_t rows_per_token, dim;
+  const int64_t* slots;
+  uint8_t* data;
+  uint8_t* scale;
+  int64_t num_pages;
+  int32_t block_size;
+};
+
+// Launchers return cudaGetLastError() after enqueueing.
+cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s);
+cudaError_t launch_fp8_quantize(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
+cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
+
+// Kernel-side limits the host validates against.
+constexpr int kMaxBatchSmem = 4096;   // sequences per call (the indexer keeps a prefix table in smem)
+constexpr int kSelTopK = 16;          // selection width the kernels are built for
+
+inline int attn_splits(int64_t rows) {
+  // split-K factor over the 16 selected blocks: enough CTAs to fill the GPU several times
+  int64_t want = (1024 + rows - 1) / rows;
+  int s = 1;
+  while (s < 16 && s < want) s <<= 1;
+  return s;
+}
+
+}  // namespace msa

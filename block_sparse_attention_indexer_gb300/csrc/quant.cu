@@ -1,0 +1,107 @@
+// NVFP4 quantise-and-insert of cache rows, and FP8 E4M3 encoding of queries.
+//
+// NVFP4: E2M1 values with one E4M3 scale per 16 elements ("vLLM liefert
+// Day-0-Unterstützung für MiniMax-M3.1-Flash", §Was ist neu in der MiniMax-M3.1-Architektur;
+// the write into the cache is the epilogue of §QKV GEMM + Norm + RoPE + KV-Insert-Fusion).
+// Rounding: scale = E4M3_rn_satfinite(amax / 6), element = E2M1_rn_satfinite(x / scale),
+// both divisions correctly rounded float32, a zero scale gives zero codes.
+#include "msa_device.cuh"
+#include "msa_kernels.h"
+
+namespace msa {
+
+// Four E2M1 codes pairs from eight floats: byte i = code(v[2i]) | code(v[2i+1]) << 4.
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float* v) {
+  uint32_t w;
+  asm("{\n"
+      " .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n"
+      "}"
+      : "=r"(w)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return w;
+}
+
+// E4M3 code of one float (round to nearest even, saturating).
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+  unsigned short h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(x));
+  return h & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2 = e4m3x2_to_f16x2(code);
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// One thread per 16-element group.
+__global__ void nvfp4_insert_kernel(QuantArgs a) {
+  const int groups_per_row = a.dim / 16;
+  const int64_t groups_per_token = static_cast<int64_t>(a.rows_per_token) * groups_per_row;
+  const int64_t total = a.n_tokens * groups_per_token;
+  for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gi < total;
+       gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tok = gi / groups_per_token;
+    const int64_t rem = gi - tok * groups_per_token;
+    const int row = static_cast<int>(rem / groups_per_row);
+    const int grp = static_cast<int>(rem - static_cast<int64_t>(row) * groups_per_row);
+    const int64_t slot = a.slots[tok];
+    if (slot < 0 || slot >= a.num_pages * a.block_size) continue;
+    const int64_t page = slot / a.block_size;
+    const int off = static_cast<int>(slot - page * a.block_size);
+
+    const float4* src = reinterpret_cast<const float4*>(a.x + (tok * a.rows_per_token + row) * a.dim + grp * 16);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float4 f = src[i];
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t scode = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+    const float scale = e4m3_to_f32(scode);
+    uint2 packed = make_uint2(0u, 0u);
+    if (scale > 0.0f) {
+      float r[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(v[i], scale);
+      packed.x = f32x8_to_e2m1x8(r);
+      packed.y = f32x8_to_e2m1x8(r + 8);
+    }
+    const int64_t row_index = (page * a.rows_per_token + row) * a.block_size + off;
+    *reinterpret_cast<uint2*>(a.data + row_index * (a.dim / 2) + grp * 8) = packed;
+    a.scale[row_index * groups_per_row + grp] = static_cast<uint8_t>(scode);
+  }
+}
+
+__global__ void fp8_quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ out) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = static_cast<uint8_t>(f32_to_e4m3(x[i]));
+}
+
+cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s) {
+  const int64_t total = a.n_tokens * a.rows_per_token * (a.dim / 16);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  nvfp4_insert_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_quantize(const float* x, int64_t n, uint8_t* out, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (n + threads - 1) / threads;
+  fp8_quantize_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0, s>>>(x, n,
+                                                                                                            out);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

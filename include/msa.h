@@ -1,0 +1,194 @@
+/*
+ * msa.h -- C ABI of the GB300 (sm_103a) MiniMax Sparse Attention decode library (libmsa.so).
+ *
+ * MSA replaces full attention with block-sparse attention.  The KV cache is split into
+ * 128-token blocks; a lightweight indexer scores every key in the context with one index
+ * query per GQA group against a single shared index-key head, max-pools the scores to
+ * one score per block, and the main attention then runs exactly, but only over the
+ * top-16 blocks, the most recent block always kept, so every query sees at most 2,048
+ * keys ("vLLM liefert Day-0-Unterstützung für MiniMax-M3.1-Flash", §MSA-Grundlagen).
+ * Both the main K/V cache and the index-key cache are NVFP4 (E2M1 values, one E4M3
+ * scale per 16 elements); queries are FP8 E4M3 (same page, §Was ist neu in der
+ * MiniMax-M3.1-Architektur and §NVIDIA-Blackwell-optimierte MSA-Kernel).
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is DEVICE memory owned by the caller; the library allocates
+ *     and frees nothing and never synchronises the device (msa_read_device_error is the
+ *     one documented exception).
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *     default stream) and returns immediately.
+ *   - Arguments are validated on the host before anything is launched; a violation
+ *     returns MSA_ERR_INVALID_ARG / MSA_ERR_UNSUPPORTED / MSA_ERR_WORKSPACE and
+ *     launches nothing.  A failed launch returns MSA_ERR_CUDA.  Output contents are
+ *     unspecified after a non-OK status.
+ *   - Data that only the device can check (block-table entries, sequence lengths) is
+ *     checked in the kernels: a bad entry sets a bit in the workspace error word, the
+ *     offending page or sequence is skipped, and nothing traps.
+ *   - Query position: token t (0 <= t < q_len) of sequence b sits at position
+ *     pos = seq_lens[b] - q_len + t (the q_len new tokens are already in the cache);
+ *     key j is visible to it iff j <= pos.  Speculative draft tokens are the q_len
+ *     tokens of one request, flattened request-major ("MiniMax M3 x vLLM：百万 token 多模态
+ *     推理的 Day-0 部署", §Decode Kernel 中的投机解码).
+ *   - seq_lens[b] == 0 marks a padding row: its outputs are defined (scores -inf,
+ *     selection -1, output 0, lse -inf) and no error is raised.
+ *
+ * Layouts (row-major; every pointer 16-byte aligned):
+ *   index-key cache  idx_data  uint8 [num_pages][128][Di/2]   idx_scale uint8 [num_pages][128][Di/16]
+ *   K (and V) cache  k_data    uint8 [num_pages][G][128][D/2] k_scale   uint8 [num_pages][G][128][D/16]
+ *     byte i of a row holds element 2i in its low nibble and element 2i+1 in its high nibble;
+ *     scale byte s of a row is the E4M3 scale of elements 16s..16s+15.
+ *   block_table      int32 [batch][max_blocks]  logical block n of sequence b -> page
+ *   seq_lens         int32 [batch]
+ *   queries q        uint8 E4M3 [batch][q_len][G*Hg][D]   (head h belongs to group h / Hg)
+ *   index queries    uint8 E4M3 [batch][q_len][G][Di]
+ *   block_scores     float [batch][q_len][G][max_blocks]
+ *   selection        int32 [batch][q_len][G][top_k]  ascending logical block ids, -1 padded
+ *   out              bfloat16 bits (uint16) [batch][q_len][G*Hg][D]
+ *   lse              float [batch][q_len][G*Hg]  natural log of the softmax denominator
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_ABI_VERSION 1
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+  MSA_ERR_UNSUPPORTED = 2,  /* a configuration this build does not implement */
+  MSA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than msa_workspace_bytes() */
+  MSA_ERR_CUDA = 4          /* a CUDA launch or query failed */
+} msa_status_t;
+
+/* Bits of the device error word (first 4 bytes of the workspace). */
+#define MSA_DEVERR_BAD_PAGE 0x1u    /* a block-table entry outside [0, num_pages) */
+#define MSA_DEVERR_BAD_SEQLEN 0x2u  /* seq_len < q_len (but > 0), or > max_blocks*128 */
+#define MSA_DEVERR_TIMEOUT 0x4u     /* a bounded wait inside a kernel gave up */
+
+/* Sparse configuration.  The pages' M3 recipe: block 128, top-16, init_blocks = 0,
+ * local_blocks = 1 ("MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署", §MSA 机制细节).
+ * This build implements exactly: num_kv_groups in 1..8, heads_per_group in 1..8,
+ * head_dim = index_dim = block_size = 128, top_k = 16, init_blocks = 0, local_blocks = 1;
+ * anything else returns MSA_ERR_UNSUPPORTED. */
+typedef struct {
+  int32_t num_kv_groups;    /* G */
+  int32_t heads_per_group;  /* Hg */
+  int32_t head_dim;         /* D */
+  int32_t index_dim;        /* Di */
+  int32_t block_size;       /* tokens per block and per cache page */
+  int32_t top_k;            /* blocks kept per (query token, KV group), recent block included */
+  int32_t init_blocks;      /* leading blocks always kept */
+  int32_t local_blocks;     /* trailing (recent) blocks always kept */
+  float softmax_scale;      /* logits = (q . k) * softmax_scale; 0 means 1/sqrt(head_dim) */
+} msa_config_t;
+
+/* The paged NVFP4 caches (device, caller-owned, read-only for decode). */
+typedef struct {
+  const uint8_t* k_data;
+  const uint8_t* k_scale;
+  const uint8_t* v_data;
+  const uint8_t* v_scale;
+  const uint8_t* idx_data;
+  const uint8_t* idx_scale;
+  int64_t num_pages;
+} msa_cache_t;
+
+/* One decode batch (device pointers; sizes on the host). */
+typedef struct {
+  const int32_t* block_table;  /* [batch][max_blocks] */
+  const int32_t* seq_lens;     /* [batch] */
+  int32_t batch;               /* 0..65535 */
+  int32_t max_blocks;          /* >= 1 */
+  int32_t q_len;               /* query tokens per sequence, >= 1 */
+} msa_batch_t;
+
+typedef enum {
+  MSA_OP_INDEXER_SCORES = 0,
+  MSA_OP_SELECT_BLOCKS = 1,
+  MSA_OP_SPARSE_ATTN = 2,
+  MSA_OP_DECODE = 3
+} msa_op_t;
+
+/* ABI version of the loaded library (MSA_ABI_VERSION). */
+int32_t msa_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* msa_status_string(msa_status_t status);
+
+/* Bytes of device workspace `op` needs for this configuration and batch (host-only
+ * arithmetic, no device access).  The workspace must be zero-filled once when it is
+ * allocated (its first 4 bytes are the device error word); after that it may be reused
+ * by every call with the same or smaller sizes.  Returns 0 for invalid arguments. */
+size_t msa_workspace_bytes(msa_op_t op, const msa_config_t* cfg, const msa_batch_t* batch);
+
+/* NVFP4 quantise-and-insert of new cache rows (the cache-write step in front of decode;
+ * the pages fuse it into the QKV GEMM epilogue: "vLLM liefert Day-0-Unterstützung für
+ * MiniMax-M3.1-Flash", §QKV GEMM + Norm + RoPE + KV-Insert-Fusion).
+ *   x        float [n_tokens][rows_per_token][dim]   (K or V: rows = G; index keys: rows = 1)
+ *   slots    int64 [n_tokens]  slot = page * block_size + offset of each token
+ *   data     uint8 [num_pages][rows_per_token][block_size][dim/2]   (written)
+ *   scale    uint8 [num_pages][rows_per_token][block_size][dim/16]  (written)
+ * For every 16 consecutive elements: scale code = E4M3(amax/6), amax/6 in float32 rounded
+ * to nearest even and saturated at 448; element code = E2M1(x/scale), x/scale in float32,
+ * rounded to nearest even, saturated at +-6, sign kept; a zero scale gives zero codes.
+ * Slots outside [0, num_pages*block_size) set nothing and are skipped. */
+msa_status_t msa_nvfp4_insert(const float* x, int64_t n_tokens, int32_t rows_per_token, int32_t dim,
+                              const int64_t* slots, uint8_t* data, uint8_t* scale, int64_t num_pages,
+                              int32_t block_size, void* stream);
+
+/* FP8 E4M3 encoding of float32 values (round to nearest even, saturating at +-448, sign kept). */
+msa_status_t msa_fp8_quantize(const float* x, int64_t n, uint8_t* out, void* stream);
+
+/* Stage 1 -- indexer score + block max-pool.
+ * block_scores[b][t][g][n] = max over visible keys j of block n of (qi[b][t][g] . key_j),
+ * exact products (E2M1 x E4M3 x E4M3) accumulated in float32; -inf where block n has no
+ * visible key (n beyond the query's own block or past the sequence end).  Entries
+ * n >= ceil(seq_len/128) are written -inf too.  Any q_len works; q_len <= 8 takes the
+ * decode kernel, larger q_len the prefill kernel.
+ * workspace: msa_workspace_bytes(MSA_OP_INDEXER_SCORES, ...). */
+msa_status_t msa_indexer_scores(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                const uint8_t* index_q, float* block_scores, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Stage 2 -- top-k block selection with the recent block forced.
+ * For each (b, t, g): r = pos / 128 is always selected; the other top_k - 1 come from the
+ * blocks n < r ranked by (score descending, index ascending; NaN below -inf); the
+ * result is sorted ascending, min(top_k, r + 1) ids, -1 padded.  Bit-exact for given
+ * scores.  No workspace. */
+msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch, const float* block_scores,
+                               int32_t* selection, void* stream);
+
+/* Stage 3 -- exact sparse GQA attention over the selected blocks (split-K over the
+ * blocks, online softmax, partial merge).  Every head h of group g attends, with
+ * logits (q . k) * softmax_scale, to the visible keys of selection[b][t][g][:];
+ * K/V are dequantised exactly from NVFP4 in the kernel.  out is rounded to bfloat16;
+ * lse may be NULL.  workspace: msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...). */
+msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                    const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Fused decode step = stage 1 + stage 2 + stage 3 on one stream, intermediate scores and
+ * selections kept in the workspace.  selection_out (may be NULL) receives a copy of the
+ * selection.  workspace: msa_workspace_bytes(MSA_OP_DECODE, ...). */
+msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                        const uint8_t* q, const uint8_t* index_q, uint16_t* out, float* lse,
+                        int32_t* selection_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Debug helper: copies the device error word out of `workspace` into *flags (this call
+ * synchronises `stream`). */
+msa_status_t msa_read_device_error(const void* workspace, uint32_t* flags, void* stream);
+
+/* Clears the device error word (asynchronous). */
+msa_status_t msa_clear_device_error(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

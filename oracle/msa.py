@@ -72,36 +72,39 @@ def query_positions(length: int, q_len: int) -> np.ndarray:
 # stage 1: indexer score + block max-pool
 # --------------------------------------------------------------------------------------
 def block_scores(qi_codes, idx_data, idx_scale, block_table, seq_lens, max_blocks: int | None = None,
-                 rows_per_matmul: int = 256) -> np.ndarray:
+                 rows_per_matmul: int = 256, tokens=None, sequences=None) -> np.ndarray:
     """Block scores S[b, t, g, n] = max over visible keys j of block n of qi[b,t,g] . k_j.
 
     qi_codes: uint8 E4M3 [B, T, G, Di].  A block with no visible key scores -inf (every
     block after the query's own block, and every block past the sequence end).
-    Returns float64 [B, T, G, max_blocks].
+    Returns float64 [B, T, G, max_blocks].  `tokens` / `sequences` restrict the work to
+    those query-token indices / sequences (the other rows stay -inf).
     """
     B, T, G, _ = qi_codes.shape
     if max_blocks is None:
         max_blocks = block_table.shape[1]
     out = np.full((B, T, G, max_blocks), -np.inf)
-    for b in range(B):
+    ts_all = np.arange(T) if tokens is None else np.asarray(sorted(tokens), dtype=np.int64)
+    step = max(1, rows_per_matmul // G)
+    for b in (range(B) if sequences is None else sequences):
         L = int(seq_lens[b])
         if L <= 0:
             continue
         keys = index_keys(idx_data, idx_scale, block_table[b], L)    # [L, Di]
         nb = -(-L // BLOCK)
         qi = E4M3_TABLE[qi_codes[b]]                                  # [T, G, Di]
-        pos = query_positions(L, T)
-        for t0 in range(0, T, max(1, rows_per_matmul // G)):
-            t1 = min(T, t0 + max(1, rows_per_matmul // G))
-            s = keys @ qi[t0:t1].reshape(-1, qi.shape[-1]).T          # [L, (t1-t0)*G]
-            s = s.reshape(L, t1 - t0, G)
-            padded = np.full((nb * BLOCK, t1 - t0, G), -np.inf)
+        pos_all = query_positions(L, T)
+        for c0 in range(0, len(ts_all), step):
+            ts = ts_all[c0:c0 + step]
+            s = keys @ qi[ts].reshape(-1, qi.shape[-1]).T             # [L, len(ts)*G]
+            s = s.reshape(L, len(ts), G)
+            padded = np.full((nb * BLOCK, len(ts), G), -np.inf)
             padded[:L] = s
             j = np.arange(nb * BLOCK)[:, None]
-            visible = j <= pos[t0:t1][None, :]                        # [nb*128, t1-t0]
+            visible = j <= pos_all[ts][None, :]                       # [nb*128, len(ts)]
             padded = np.where(visible[:, :, None], padded, -np.inf)
-            pooled = padded.reshape(nb, BLOCK, t1 - t0, G).max(axis=1)   # [nb, t, G]
-            out[b, t0:t1, :, :nb] = pooled.transpose(1, 2, 0)
+            pooled = padded.reshape(nb, BLOCK, len(ts), G).max(axis=1)   # [nb, len(ts), G]
+            out[b, ts, :, :nb] = pooled.transpose(1, 2, 0)
     return out
 
 
@@ -145,24 +148,27 @@ def select_blocks(scores, seq_lens, top_k: int = TOP_K) -> np.ndarray:
 # stage 3: exact sparse GQA attention over the selected blocks
 # --------------------------------------------------------------------------------------
 def sparse_attention(q_codes, k_data, k_scale, v_data, v_scale, block_table, seq_lens, sel,
-                     heads_per_group: int, softmax_scale: float | None = None):
+                     heads_per_group: int, softmax_scale: float | None = None, tokens=None, sequences=None):
     """Attention of every query head over the visible keys of its group's selected blocks.
 
     q_codes: uint8 E4M3 [B, T, H, D]; sel: int32 [B, T, G, k].
     Returns (out float64 [B, T, H, D], lse float64 [B, T, H]) with lse the natural log of
-    the softmax denominator including the row max.
+    the softmax denominator including the row max.  `tokens` / `sequences` restrict the
+    work to those rows (the others stay 0 / -inf).
     """
     B, T, H, D = q_codes.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     out = np.zeros((B, T, H, D))
     lse = np.full((B, T, H), -np.inf)
-    for b in range(B):
+    for b in (range(B) if sequences is None else sequences):
         L = int(seq_lens[b])
         if L <= 0:
             continue
         q = E4M3_TABLE[q_codes[b]]                                     # [T, H, D]
-        for t, pos in enumerate(query_positions(L, T)):
+        positions = query_positions(L, T)
+        for t in (range(T) if tokens is None else tokens):
+            pos = int(positions[t])
             for g in range(sel.shape[2]):
                 blocks = [int(n) for n in sel[b, t, g] if n >= 0]
                 K = kv_rows(k_data, k_scale, block_table[b], g, blocks)
