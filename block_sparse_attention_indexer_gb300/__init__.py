@@ -27,5 +27,6 @@ from .binding import (  # noqa: F401
     msa_read_device_error,
     msa_select_blocks,
     msa_sparse_attn_decode,
+    msa_sparse_attn_decode_noalloc,
     msa_workspace_bytes,
 )

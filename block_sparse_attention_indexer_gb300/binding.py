@@ -4,7 +4,7 @@ Argument marshalling only: every function takes torch tensors, checks dtype / de
 contiguity, passes data pointers and the current CUDA stream to the C entry point of the
 same name, and raises MsaError on a non-OK status.  All compute happens in the library's
 CUDA kernels; there is no Python or CPU fallback.  If libmsa.so has not been built the
-import fails loudly (build with `python -m block_sparse_attention_indexer_gb300.build`).
+import fails loudly (build with `python block_sparse_attention_indexer_gb300/build.py`).
 """
 from __future__ import annotations
 
@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libmsa.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m block_sparse_attention_indexer_gb300.build` "
+        f"{LIB_PATH} is missing: build it with `python block_sparse_attention_indexer_gb300/build.py` "
         "(the MSA path has no CPU fallback)")
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -62,6 +62,7 @@ _SIGS = {
     "msa_select_blocks": (ctypes.c_int, [_CP, _CB, _P, _P, _P]),
     "msa_sparse_attn_decode": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msa_decode": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "msa_sparse_attn_decode_noalloc": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P]),
     "msa_read_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "msa_clear_device_error": (ctypes.c_int, [_P, _P]),
 }
@@ -225,6 +226,17 @@ def msa_sparse_attn_decode(cfg: Config, cache: PagedCache, batch: Batch, q: torc
         cfg.c(), cache.c(), batch.c(), _ptr(q, torch.uint8, "q"), _ptr(selection, torch.int32, "selection"),
         _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def msa_sparse_attn_decode_noalloc(cfg: Config, cache: PagedCache, batch: Batch, q: torch.Tensor,
+                                   selection: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor],
+                                   stream=None):
+    """msa_sparse_attn_decode without a workspace, for callers that cannot allocate device
+    memory: the scratch is the library's own 8 MiB device array (see include/msa.h).  Calls
+    that overlap on the GPU share that array and race."""
+    _check("msa_sparse_attn_decode_noalloc", _lib.msa_sparse_attn_decode_noalloc(
+        cfg.c(), cache.c(), batch.c(), _ptr(q, torch.uint8, "q"), _ptr(selection, torch.int32, "selection"),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream)))
 
 
 def msa_decode(cfg: Config, cache: PagedCache, batch: Batch, q: torch.Tensor, index_q: torch.Tensor,

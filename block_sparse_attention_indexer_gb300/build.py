@@ -2,7 +2,7 @@
 
 Each .cu file compiles in parallel to an object under _build/, then one nvcc link makes
 block_sparse_attention_indexer_gb300/libmsa.so.  Objects are rebuilt when their source or
-any header changed.  Usage: python -m block_sparse_attention_indexer_gb300.build [-v]
+any header changed.  Usage: python block_sparse_attention_indexer_gb300/build.py [-v] [-f]
 """
 from __future__ import annotations
 
@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa.so")
-SOURCES = ["api.cu", "quant.cu", "indexer.cu", "select.cu", "attention.cu"]
+SOURCES = ["api.cu", "quant.cu", "indexer.cu", "select.cu", "attention.cu", "noalloc.cu"]
 HEADERS = ["msa_device.cuh", "msa_kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]

@@ -180,6 +180,28 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
                         const uint8_t* q, const uint8_t* index_q, uint16_t* out, float* lse,
                         int32_t* selection_out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The stage-3 sparse attention of msa_sparse_attn_decode for callers that cannot allocate
+ * device memory, or cannot hand the library a workspace: for example a plugin inside a host
+ * application whose device memory all belongs to that application's own pool, or code that
+ * must not allocate between decode steps.  The source pages have no counterpart; this is a
+ * deployment convenience.
+ * Same arguments and results as msa_sparse_attn_decode, minus the workspace: the scratch
+ * (split partial states and the device error word) lives in one library-owned device array
+ * of 8 MiB, which every GPU that loads the library holds until the process exits.  Nothing
+ * is allocated or freed.
+ *   - Batches whose msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...) exceeds 8 MiB are rejected
+ *     with MSA_ERR_WORKSPACE before anything is launched (the five reference workloads all
+ *     fit; 256 rows of (sequence, token, group) with 8 heads need 4.3 MB).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents: calls that can
+ *     overlap on the GPU (different streams, or different host threads, on one device) race
+ *     and must be serialised by the caller.  The error word is cleared at the start of each
+ *     call and is not readable from outside. */
+msa_status_t msa_sparse_attn_decode_noalloc(const msa_config_t* cfg, const msa_cache_t* cache,
+                                            const msa_batch_t* batch, const uint8_t* q, const int32_t* selection,
+                                            uint16_t* out, float* lse, void* stream);
+
 /* Debug helper: copies the device error word out of `workspace` into *flags (this call
  * synchronises `stream`). */
 msa_status_t msa_read_device_error(const void* workspace, uint32_t* flags, void* stream);
