@@ -39,6 +39,35 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = {
+    "indexer_kernel": ["indexer.cu", "msa_device.cuh", "msa_kernels.h"],
+    "attention_kernel": ["attention.cu", "msa_device.cuh", "msa_kernels.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "block_sparse_attention_indexer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, or None when the
+    kernel's sources changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)[kernel]
+    except Exception:
+        return None
+    if entry.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    return entry.get("bytes_per_launch", {}).get(workload)
+
+
 class ClockSampler:
     """nvidia-smi SM clock / throttle-reason sampling during the timed region."""
 
@@ -334,15 +363,7 @@ def run_ours(args):
     while splits < 16 and splits < -(-1024 // rows):
         splits <<= 1
     launches_per_step = 3 + (1 if splits > 1 else 0)
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                tj = json.load(f)
-            traffic = tj.get(w.name, {}).get("indexer_kernel_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = measured_traffic("indexer_kernel", w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

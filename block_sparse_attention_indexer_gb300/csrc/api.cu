@@ -71,11 +71,7 @@ size_t scores_bytes(const msa_config_t* c, const msa_batch_t* b) {
 size_t sel_bytes(const msa_config_t* c, const msa_batch_t* b) {
   return align_up(static_cast<size_t>(rows_tg(b, c)) * kSelTopK * sizeof(int32_t));
 }
-size_t partial_bytes(const msa_config_t* c, const msa_batch_t* b) {
-  const int splits = attn_splits(rows_tg(b, c));
-  if (splits == 1) return 0;
-  return align_up(static_cast<size_t>(rows_tg(b, c)) * c->heads_per_group * splits * (128 + 2) * sizeof(float));
-}
+size_t partial_bytes() { return align_up(attn_partial_bytes()); }
 
 float scale_log2(const msa_config_t* c) {
   const float sm = c->softmax_scale > 0.0f ? c->softmax_scale : 1.0f / std::sqrt(static_cast<float>(c->head_dim));
@@ -136,7 +132,6 @@ AttnArgs attn_args(const msa_config_t* cfg, const msa_cache_t* cache, const msa_
   a.out = out;
   a.lse = lse;
   a.partial = partial;
-  a.splits = attn_splits(rows_tg(batch, cfg));
   a.scale_log2 = scale_log2(cfg);
   a.err = err;
   return a;
@@ -164,9 +159,8 @@ size_t msa_workspace_bytes(msa_op_t op, const msa_config_t* cfg, const msa_batch
   switch (op) {
     case MSA_OP_INDEXER_SCORES: return kErrBytes;
     case MSA_OP_SELECT_BLOCKS: return 0;
-    case MSA_OP_SPARSE_ATTN: return kErrBytes + partial_bytes(cfg, batch);
-    case MSA_OP_DECODE:
-      return kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch) + partial_bytes(cfg, batch);
+    case MSA_OP_SPARSE_ATTN: return kErrBytes + partial_bytes();
+    case MSA_OP_DECODE: return kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch) + partial_bytes();
   }
   return 0;
 }
@@ -231,10 +225,12 @@ msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* 
   if (workspace == nullptr || workspace_bytes < msa_workspace_bytes(MSA_OP_SPARSE_ATTN, cfg, batch) ||
       !aligned16(workspace))
     return MSA_ERR_WORKSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MSA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* partial = partial_bytes(cfg, batch) ? reinterpret_cast<float*>(ws + kErrBytes) : nullptr;
+  float* partial = reinterpret_cast<float*>(ws + kErrBytes);
   AttnArgs a = attn_args(cfg, cache, batch, q, selection, out, lse, partial, reinterpret_cast<uint32_t*>(ws));
-  return cuda_status(launch_attention(a, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_attention(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
@@ -259,12 +255,10 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
   int32_t* sel = selection_out != nullptr
                      ? selection_out
                      : reinterpret_cast<int32_t*>(ws + kErrBytes + scores_bytes(cfg, batch));
-  float* partial = partial_bytes(cfg, batch)
-                       ? reinterpret_cast<float*>(ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch))
-                       : nullptr;
+  float* partial = reinterpret_cast<float*>(ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch));
   cudaError_t e = launch_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
   if (e == cudaSuccess) e = launch_select(select_args(cfg, batch, scores, sel), s);
-  if (e == cudaSuccess) e = launch_attention(attn_args(cfg, cache, batch, q, sel, out, lse, partial, err), s);
+  if (e == cudaSuccess) e = launch_attention(attn_args(cfg, cache, batch, q, sel, out, lse, partial, err), sms, s);
   return cuda_status(e);
 }
 

@@ -1,5 +1,4 @@
-// Stage 3 of MSA decode: exact sparse GQA attention over the selected blocks, split-K
-// over the blocks with an online-softmax merge.
+// Stage 3 of MSA decode: exact sparse GQA attention over the selected blocks.
 //
 // Every query head of a KV group attends exactly, and only, to the selected blocks of that
 // group ("vLLM liefert Day-0-Unterstützung für MiniMax-M3.1-Flash", §MSA-Grundlagen, Fig. 1);
@@ -9,20 +8,24 @@
 // work (same page, §MiniMax 稀疏注意力后端 and §Decode 执行).
 //
 // Design (GB300):
-//   * grid (split, group, sequence x query token); each CTA stages its <= 4 selected
-//     pages of K and V (18 KB each: E2M1 bytes + E4M3 scales of one KV head) with bulk
-//     async copies, 4 warps each take one 32-key quarter of every page;
-//   * QK runs transposed, S^T = K Q^T on mma.sync m16n8k16 with keys as M and the (up to
-//     8) heads of the group as N, so the heads fill the N=8 tile with no padding; K is
-//     dequantised straight into A registers (cvt e2m1x2 -> f16x2, times the f16 block scale:
-//     exact), the FP8 queries widen exactly to f16;
-//   * the probabilities are packed to f16 and transposed in registers (movmatrix) into the
-//     B operand of O^T = V^T P^T, whose A operand is V^T built from two keys' bytes with a
-//     nibble transpose (LOP3), again exact -- no shared-memory round trip for either
-//     operand;
-//   * softmax in the exp2 domain with the scale folded into one multiply; a split's
-//     partial state (o, m, l) is merged across warps in shared memory and across splits
-//     by merge_kernel (o = sum e^{m_s-M} o_s / sum e^{m_s-M} l_s).
+//   * persistent: one CTA per SM, three independent teams of four warps.  The (row = (sequence,
+//     token, group), selection entry) pairs, 16 per row, are split into equal contiguous
+//     ranges, one per team, so every team streams the same number of 18 KB pages (K and V of
+//     one KV head, E2M1 bytes + E4M3 scales) whatever the selections;
+//   * in each team one warp produces: it resolves entries (selection -> block table -> page)
+//     32 at a time, one per lane, and streams the pages through a 3-slot shared-memory ring
+//     with bulk async copies (cp.async.bulk), full / empty mbarriers and the item's metadata
+//     in shared memory; a row with no page to attend to still gets one marker item;
+//   * every warp of the team consumes every page, each on its own 32-key quarter: QK runs
+//     transposed, S^T = K Q^T on mma.sync m16n8k16 (keys as M, the <= 8 heads of the group
+//     as N, so the heads fill the N=8 tile), an online softmax in the exp2 domain, then
+//     O^T += V^T P^T: P is packed to f16 and transposed in registers (movmatrix) into the B
+//     operand, V^T is built from two keys' bytes by a nibble transpose.  K and V are
+//     dequantised exactly (cvt e2m1x2 -> f16x2 times the f16 block scale);
+//   * at a row change the four warps merge their states through shared memory (mbarrier
+//     handshakes, every wait bounded); a row wholly inside the team's range is written out
+//     at once, a row cut by a range boundary leaves a partial state (o, m, l) in one of two
+//     slots of the team, combined by merge_kernel: o = sum e^{m_s-M} o_s / sum e^{m_s-M} l_s.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -31,296 +34,513 @@
 
 namespace msa {
 
-constexpr int kAttnWarps = 4;
-constexpr int kAttnSlots = 4;
+constexpr int kTeams = 3;                                 // teams per CTA
+constexpr int kTW = 4;                                    // warps per team (one 32-key quarter each)
+constexpr int kAW = kTeams * kTW;                         // warps per CTA
+constexpr int kTSl = 3;                                   // page slots per team
 constexpr int kSlotBytes = 2 * (kPageData + kPageScale);  // K data | K scales | V data | V scales
-constexpr int kPartialStride = kDim + 2;                  // o[128], m (log2 units), l
+constexpr int kHeadsMax = 8;
+constexpr int kRedFloats = kHeadsMax * kDim + 2 * kHeadsMax;   // one warp's o[8][128], m[8], l[8]
+constexpr int kSlotFloats = kHeadsMax * (kDim + 2);             // one partial slot: [8][o 128, m, l]
 constexpr float kLn2 = 0.69314718055994530942f;
 
-__device__ __forceinline__ void store_out(const AttnArgs& a, int64_t head_row, int d, float num, float den,
+// per team: slots, merge area, item metadata, barriers
+struct TeamBars {
+  uint64_t full[kTSl];   // a page (or a marker item) is in the slot: 1 arrive (+ copy bytes)
+  uint64_t empty[kTSl];  // every warp of the team is done with the slot: kTW arrives
+  uint64_t merged;       // every warp wrote its segment state: kTW arrives
+  uint64_t freed;        // every warp finished reading the merge area: kTW arrives
+};
+struct ItemMeta {
+  int64_t row;  // row of the item, -1 = end of the team's items
+  int blk;      // logical block (page items)
+  int page;     // page id, -1 = no page (a row with nothing to attend to)
+};
+
+__host__ __device__ constexpr size_t attn_smem_bytes() {
+  return static_cast<size_t>(kTeams) * kTSl * kSlotBytes +
+         static_cast<size_t>(kAW) * kRedFloats * sizeof(float) +
+         static_cast<size_t>(kTeams) * kTSl * sizeof(ItemMeta) + static_cast<size_t>(kTeams) * sizeof(TeamBars);
+}
+
+__host__ __device__ __forceinline__ int64_t range_lo(int64_t E, int c, int NC) { return E * c / NC; }
+__host__ __device__ __forceinline__ int owner_of(int64_t E, int64_t x, int NC) {
+  return static_cast<int>(((x + 1) * NC - 1) / E);
+}
+
+struct RowInfo {
+  int b, t, g, r, L;
+  bool ok;
+  int64_t head_row0;
+};
+
+__device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int64_t row) {
+  RowInfo ri;
+  const int T = a.q_len, G = a.groups;
+  ri.b = static_cast<int>(row / (static_cast<int64_t>(T) * G));
+  ri.t = static_cast<int>((row / G) % T);
+  ri.g = static_cast<int>(row % G);
+  ri.L = a.seq_lens[ri.b];
+  ri.ok = ri.L > 0 && ri.L >= T && ri.L <= static_cast<int64_t>(a.max_blocks) * kBlock;
+  ri.r = ri.ok ? (ri.L - T + ri.t) / kBlock : -1;
+  ri.head_row0 = (row / G) * (static_cast<int64_t>(G) * a.heads_per_group) + static_cast<int64_t>(ri.g) *
+                 a.heads_per_group;
+  return ri;
+}
+
+// Resolves entries x = first + stride*(base + lane) (lane-parallel): page id (or -1 if the
+// entry is empty, past the recent block, or its block-table entry is bad) and block index.
+__device__ __forceinline__ void resolve_batch(const AttnArgs& a, int64_t first, int stride, int base, int count,
+                                              int lane, int& page, int& blk) {
+  page = -1;
+  blk = -1;
+  const int k = base + lane;
+  if (k < count) {
+    const int64_t x = first + static_cast<int64_t>(stride) * k;
+    const int64_t row = x / kTopK;
+    const RowInfo ri = row_info(a, row);
+    const int n = a.selection[x];
+    if (ri.ok && n >= 0 && n <= ri.r) {
+      const int p = a.block_table[static_cast<int64_t>(ri.b) * a.max_blocks + n];
+      if (p >= 0 && p < a.num_pages) {
+        page = p;
+        blk = n;
+      } else {
+        flag_error(a.err, MSA_DEVERR_BAD_PAGE);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void load_q_raw(const AttnArgs& a, int64_t head_row0, bool ok, int gq, int t4, uint4& q0,
+                                           uint4& q1) {
+  if (ok && gq < a.heads_per_group) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.q + (head_row0 + gq) * kDim + 32 * t4);
+    q0 = __ldg(src);
+    q1 = __ldg(src + 1);
+  } else {
+    q0 = q1 = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void q_fragments(const uint4& q0, const uint4& q1, uint32_t (&bq)[8][2]) {
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    bq[s][0] = e4m3x2_to_f16x2(w[s]);
+    bq[s][1] = e4m3x2_to_f16x2(w[s] >> 16);
+  }
+}
+
+// One 32-key quarter (qk) of one page (128 keys of one KV head) into the warp's state.
+__device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n, int r, int pos, float scale_log2,
+                                               int gq, int t4, const uint32_t (&bq)[8][2], float (&m_run)[2],
+                                               float (&l_run)[2], float (&o)[8][4]) {
+  const uint8_t* ks = kd + kPageData;
+  const uint8_t* vd = ks + kPageScale;
+  const uint8_t* vs = vd + kPageData;
+  const bool recent = (n == r);
+  // ---- S^T = K Q^T for 32 keys (two 16-key tiles)
+  float x[2][4];
+#pragma unroll
+  for (int mq = 0; mq < 2; ++mq) {
+    const int r0 = qk * 32 + mq * 16 + gq, r1 = r0 + 8;
+    const uint4 d0 = lds128(kd + r0 * kRowBytes + 16 * t4);
+    const uint4 d1 = lds128(kd + r1 * kRowBytes + 16 * t4);
+    const uint32_t s0 = lds16(ks + r0 * kRowScales + 2 * t4);
+    const uint32_t s1 = lds16(ks + r1 * kRowScales + 2 * t4);
+    const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
+    const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
+    const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
+    const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+      e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
+      e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
+      const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
+      x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
+      y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
+      mma_f16_16816(acc[0], x0, y0, x1, y1, bq[2 * w][0], bq[2 * w][1]);
+      mma_f16_16816(acc[1], x2, y2, x3, y3, bq[2 * w + 1][0], bq[2 * w + 1][1]);
+    }
+    const int j0 = n * kBlock + r0, j1 = j0 + 8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[mq][e] = (acc[0][e] + acc[1][e]) * scale_log2;
+    if (recent) {
+      if (j0 > pos) x[mq][0] = x[mq][1] = -INFINITY;
+      if (j1 > pos) x[mq][2] = x[mq][3] = -INFINITY;
+    }
+  }
+
+  // ---- online softmax per head column (2*t4 + e)
+  float p[2][4], alpha[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float mx = fmaxf(fmaxf(x[0][e], x[0][e + 2]), fmaxf(x[1][e], x[1][e + 2]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float m_new = fmaxf(m_run[e], mx);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    alpha[e] = exp2f(m_run[e] - m_use);
+    m_run[e] = m_new;
+    float sum = 0.f;
+#pragma unroll
+    for (int mq = 0; mq < 2; ++mq) {
+      p[mq][e] = exp2f(x[mq][e] - m_use);
+      p[mq][e + 2] = exp2f(x[mq][e + 2] - m_use);
+      sum += p[mq][e] + p[mq][e + 2];
+    }
+    l_run[e] = l_run[e] * alpha[e] + sum;
+  }
+  // rescale the output only when some head's running maximum moved (warp-uniform test)
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= alpha[0];
+      o[mt][2] *= alpha[0];
+      o[mt][1] *= alpha[1];
+      o[mt][3] *= alpha[1];
+    }
+  }
+
+  // ---- O^T += V^T P^T, one 16-key k-step per QK tile
+#pragma unroll
+  for (int mq = 0; mq < 2; ++mq) {
+    const uint32_t b0 = movmatrix_trans(pack_f16x2(p[mq][0], p[mq][1]));
+    const uint32_t b1 = movmatrix_trans(pack_f16x2(p[mq][2], p[mq][3]));
+    const int ka = qk * 32 + mq * 16 + 2 * t4;  // keys ka, ka+1, ka+8, ka+9
+    const uint2 va = lds64(vd + ka * kRowBytes + 8 * gq);
+    const uint2 vb = lds64(vd + (ka + 1) * kRowBytes + 8 * gq);
+    const uint2 vc = lds64(vd + (ka + 8) * kRowBytes + 8 * gq);
+    const uint2 ve = lds64(vd + (ka + 9) * kRowBytes + 8 * gq);
+    const uint32_t sab = e4m3x2_to_f16x2(lds8(vs + ka * kRowScales + gq) |
+                                         (lds8(vs + (ka + 1) * kRowScales + gq) << 8));
+    const uint32_t scd = e4m3x2_to_f16x2(lds8(vs + (ka + 8) * kRowScales + gq) |
+                                         (lds8(vs + (ka + 9) * kRowScales + gq) << 8));
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+      const uint32_t wa = hw ? va.y : va.x, wb = hw ? vb.y : vb.x;
+      const uint32_t wc = hw ? vc.y : vc.x, we = hw ? ve.y : ve.x;
+      // byte i of lo*: low nibbles of (key a, key b); of hi*: their high nibbles
+      const uint32_t lo_ab = (wa & 0x0F0F0F0Fu) | ((wb & 0x0F0F0F0Fu) << 4);
+      const uint32_t hi_ab = ((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u);
+      const uint32_t lo_ce = (wc & 0x0F0F0F0Fu) | ((we & 0x0F0F0F0Fu) << 4);
+      const uint32_t hi_ce = ((wc >> 4) & 0x0F0F0F0Fu) | (we & 0xF0F0F0F0u);
+      uint32_t la[4], ha[4], lc[4], hc[4];
+      e2m1x8_to_f16x2(lo_ab, la[0], la[1], la[2], la[3]);
+      e2m1x8_to_f16x2(hi_ab, ha[0], ha[1], ha[2], ha[3]);
+      e2m1x8_to_f16x2(lo_ce, lc[0], lc[1], lc[2], lc[3]);
+      e2m1x8_to_f16x2(hi_ce, hc[0], hc[1], hc[2], hc[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int mt = hw * 4 + i;  // output dims 16*gq + 2*mt (+1)
+        mma_f16_16816(o[mt], hmul2(la[i], sab), hmul2(ha[i], sab), hmul2(lc[i], scd), hmul2(hc[i], scd), b0, b1);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void write_out(const AttnArgs& a, int64_t head_row, int d, float num, float den,
                                           float M) {
   const float v = den > 0.f ? num / den : 0.f;
   a.out[head_row * kDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   if (d == 0 && a.lse != nullptr) a.lse[head_row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
-__global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAW * 32, 1) attention_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kAttnSlots * kSlotBytes);
-  __shared__ int s_blk[kTopK], s_page[kTopK], s_nblk;
+  float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(kTeams) * kTSl * kSlotBytes);
+  ItemMeta* meta = reinterpret_cast<ItemMeta*>(red + kAW * kRedFloats);
+  TeamBars* tbars = reinterpret_cast<TeamBars*>(meta + kTeams * kTSl);
+
+  // launched as a programmatic dependent of the previous kernel on the stream (the
+  // selection): wait for it and its memory before touching global memory
+  grid_dependency_wait();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, t4 = lane & 3;
-  const int split = blockIdx.x, grp = blockIdx.y;
-  const int T = a.q_len, G = a.groups, Hg = a.heads_per_group, H = G * Hg;
-  const int b = blockIdx.z / T, t = blockIdx.z % T;
-  const int64_t head_row0 = (static_cast<int64_t>(b) * T + t) * H + grp * Hg;
-  const int L = a.seq_lens[b];
-  const bool seq_ok = L > 0 && L >= T && L <= static_cast<int64_t>(a.max_blocks) * kBlock;
-  const int pos = L - T + t;
-  const int r = seq_ok ? pos / kBlock : -1;
-  const int bps = kTopK / a.splits;
+  const int team = warp / kTW, wt = warp % kTW;
+  const int Hg = a.heads_per_group;
+  const int NT = gridDim.x * kTeams, tt = blockIdx.x * kTeams + team;
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
+  const int64_t E = rows * kTopK;
+  const int64_t x0 = range_lo(E, tt, NT), x1 = range_lo(E, tt + 1, NT);
+  const int64_t R0 = x0 / kTopK;
 
-  if (tid == 0) {
-    int cnt = 0;
-    if (seq_ok) {
-      const int32_t* sel = a.selection + ((static_cast<int64_t>(b) * T + t) * G + grp) * kTopK + split * bps;
-      for (int i = 0; i < bps; ++i) {
-        const int n = sel[i];
-        if (n < 0 || n > r) continue;
-        const int page = a.block_table[static_cast<int64_t>(b) * a.max_blocks + n];
-        if (page < 0 || page >= a.num_pages) {
-          flag_error(a.err, MSA_DEVERR_BAD_PAGE);
-          continue;
-        }
-        s_blk[cnt] = n;
-        s_page[cnt] = page;
-        ++cnt;
-      }
+  uint8_t* my_slots = smem + static_cast<size_t>(team) * kTSl * kSlotBytes;
+  ItemMeta* my_meta = meta + team * kTSl;
+  TeamBars* tb = tbars + team;
+  float* team_red = red + team * kTW * kRedFloats;
+  if (wt == 0 && lane == 0) {
+    for (int i = 0; i < kTSl; ++i) {
+      mbar_init(&tb->full[i], 1);
+      mbar_init(&tb->empty[i], kTW);
     }
-    s_nblk = cnt;
-    for (int i = 0; i < kAttnSlots; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&tb->merged, kTW);
+    mbar_init(&tb->freed, kTW);
     fence_mbar_init();
   }
   __syncthreads();
-  const int nblk = s_nblk;
 
-  // B fragments of QK (k = dim, n = head): head gq, dims 32*t4 + 4s .. +3 for k-step s
-  uint32_t bq[8][2];
-  if (gq < Hg && seq_ok) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.q + (head_row0 + gq) * kDim + 32 * t4);
-    const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      bq[s][0] = e4m3x2_to_f16x2(w[s]);
-      bq[s][1] = e4m3x2_to_f16x2(w[s] >> 16);
+  // ---- producer (warp 0 of the team): entries of [x0, x1) in order; an item per page to
+  // attend to, one marker item for a row segment with none, and a final end item
+  const int64_t nk = x1 - x0;
+  int64_t pk = 0;
+  int pb = -1, p_page = -1, p_blk = -1;
+  bool seg_any = false, end_sent = false;
+  int produced = 0;
+  auto produce_one = [&]() {
+    const int slot = produced % kTSl;
+    while (pk < nk) {
+      const int bi = static_cast<int>(pk >> 5);
+      if (bi != pb) {
+        resolve_batch(a, x0, 1, bi * 32, static_cast<int>(nk), lane, p_page, p_blk);
+        pb = bi;
+      }
+      const int page = __shfl_sync(0xffffffffu, p_page, static_cast<int>(pk & 31));
+      const int blk = __shfl_sync(0xffffffffu, p_blk, static_cast<int>(pk & 31));
+      const int64_t x = x0 + pk;
+      ++pk;
+      const bool last_in_seg = ((x + 1) % kTopK == 0) || (x + 1 == x1);
+      const bool emit = page >= 0 || (last_in_seg && !seg_any);
+      seg_any = last_in_seg ? false : (seg_any || page >= 0);
+      if (!emit) continue;
+      if (lane == 0) {
+        uint64_t* bar = &tb->full[slot];
+        my_meta[slot].row = x / kTopK;
+        my_meta[slot].blk = blk;
+        my_meta[slot].page = page;
+        if (page >= 0) {
+          uint8_t* dst = my_slots + slot * kSlotBytes;
+          const int64_t pg = static_cast<int64_t>(page) * a.groups + (x / kTopK) % a.groups;
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(bar, kSlotBytes);
+          bulk_g2s(dst, a.k_data + pg * kPageData, kPageData, bar);
+          bulk_g2s(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar);
+          bulk_g2s(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar);
+          bulk_g2s(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar);
+        } else {
+          mbar_arrive(bar);
+        }
+      }
+      ++produced;
+      return;
     }
-  } else {
-#pragma unroll
-    for (int s = 0; s < 8; ++s) bq[s][0] = bq[s][1] = 0u;
-  }
+    if (!end_sent) {
+      if (lane == 0) {
+        my_meta[slot].row = -1;
+        my_meta[slot].blk = -1;
+        my_meta[slot].page = -1;
+        mbar_arrive(&tb->full[slot]);
+      }
+      end_sent = true;
+      ++produced;
+    }
+  };
+  if (wt == 0)
+    for (int s = 0; s < kTSl && !end_sent; ++s) produce_one();
 
+  // ---- consumers (all four warps)
+  int consumed = 0, nseg = 0;
+  int64_t cur_row = -2;
+  RowInfo ri = {};
+  int pos = 0;
+  uint32_t bq[8][2] = {};
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  float o[8][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float o[8][4] = {};
+  bool failed = false;
 
-  for (int base = 0, round = 0; base < nblk; base += kAttnSlots, ++round) {
-    const int nr = min(kAttnSlots, nblk - base);
-    if (tid == 0) {
-      for (int i = 0; i < nr; ++i) {
-        uint8_t* slot = smem + i * kSlotBytes;
-        const int64_t pg = static_cast<int64_t>(s_page[base + i]) * G + grp;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[i], kSlotBytes);
-        bulk_g2s(slot, a.k_data + pg * kPageData, kPageData, &bars[i]);
-        bulk_g2s(slot + kPageData, a.k_scale + pg * kPageScale, kPageScale, &bars[i]);
-        bulk_g2s(slot + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, &bars[i]);
-        bulk_g2s(slot + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, &bars[i]);
-      }
+  auto finalize = [&](int64_t R) -> bool {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = l_run[e];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      l_run[e] = v;
     }
-    for (int i = 0; i < nr; ++i) {
-      if (!mbar_wait_warp(&bars[i], round & 1)) {
-        if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
-        continue;
-      }
-      const uint8_t* kd = smem + i * kSlotBytes;
-      const uint8_t* ks = kd + kPageData;
-      const uint8_t* vd = ks + kPageScale;
-      const uint8_t* vs = vd + kPageData;
-      const int n = s_blk[base + i];
-      const bool recent = (n == r);
-
-      // ---- S^T = K Q^T for this warp's 32 keys (two 16-key tiles)
-      float x[2][4];
+    if (nseg > 0 && !mbar_wait_warp(&tb->freed, (nseg - 1) & 1)) return false;
+    float* my_red = team_red + wt * kRedFloats;
 #pragma unroll
-      for (int mq = 0; mq < 2; ++mq) {
-        const int r0 = warp * 32 + mq * 16 + gq, r1 = r0 + 8;
-        const uint4 d0 = lds128(kd + r0 * kRowBytes + 16 * t4);
-        const uint4 d1 = lds128(kd + r1 * kRowBytes + 16 * t4);
-        const uint32_t s0 = lds16(ks + r0 * kRowScales + 2 * t4);
-        const uint32_t s1 = lds16(ks + r1 * kRowScales + 2 * t4);
-        const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
-        const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
-        const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
-        const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = 16 * gq + 2 * mt;
+      *reinterpret_cast<float2*>(my_red + (2 * t4) * kDim + d0) = make_float2(o[mt][0], o[mt][2]);
+      *reinterpret_cast<float2*>(my_red + (2 * t4 + 1) * kDim + d0) = make_float2(o[mt][1], o[mt][3]);
+    }
+    if (gq == 0) {
+      my_red[kHeadsMax * kDim + 2 * t4] = m_run[0];
+      my_red[kHeadsMax * kDim + 2 * t4 + 1] = m_run[1];
+      my_red[kHeadsMax * kDim + kHeadsMax + 2 * t4] = l_run[0];
+      my_red[kHeadsMax * kDim + kHeadsMax + 2 * t4 + 1] = l_run[1];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tb->merged);
+    if (!mbar_wait_warp(&tb->merged, nseg & 1)) return false;
+    const bool whole = R * kTopK >= x0 && (R + 1) * kTopK <= x1;
+    float* slot_part = whole ? nullptr : a.partial + static_cast<int64_t>(2 * tt + (R == R0 ? 0 : 1)) * kSlotFloats;
+    const int d = wt * 32 + lane;  // each warp merges 32 of the 128 dims
+    for (int h = 0; h < Hg; ++h) {
+      float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-          e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
-          e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
-          const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
-          x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
-          y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
-          mma_f16_16816(acc, x0, y0, x1, y1, bq[2 * w][0], bq[2 * w][1]);
-          mma_f16_16816(acc, x2, y2, x3, y3, bq[2 * w + 1][0], bq[2 * w + 1][1]);
-        }
-        const int j0 = n * kBlock + r0, j1 = j0 + 8;
+      for (int w = 0; w < kTW; ++w) M = fmaxf(M, team_red[w * kRedFloats + kHeadsMax * kDim + h]);
+      float num = 0.f, den = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[mq][e] = acc[e] * a.scale_log2;
-        if (recent) {
-          if (j0 > pos) x[mq][0] = x[mq][1] = -INFINITY;
-          if (j1 > pos) x[mq][2] = x[mq][3] = -INFINITY;
-        }
-      }
-
-      // ---- online softmax per head column (2*t4 + e)
-      float p[2][4];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float mx = fmaxf(fmaxf(x[0][e], x[0][e + 2]), fmaxf(x[1][e], x[1][e + 2]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[e], mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = exp2f(m_run[e] - m_use);
-        m_run[e] = m_new;
-        float sum = 0.f;
-#pragma unroll
-        for (int mq = 0; mq < 2; ++mq) {
-          p[mq][e] = exp2f(x[mq][e] - m_use);
-          p[mq][e + 2] = exp2f(x[mq][e + 2] - m_use);
-          sum += p[mq][e] + p[mq][e + 2];
-        }
-        l_run[e] = l_run[e] * alpha + sum;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][e] *= alpha;
-          o[mt][e + 2] *= alpha;
-        }
-      }
-
-      // ---- O^T += V^T P^T, one 16-key k-step per QK tile
-#pragma unroll
-      for (int mq = 0; mq < 2; ++mq) {
-        const uint32_t b0 = movmatrix_trans(pack_f16x2(p[mq][0], p[mq][1]));
-        const uint32_t b1 = movmatrix_trans(pack_f16x2(p[mq][2], p[mq][3]));
-        const int ka = warp * 32 + mq * 16 + 2 * t4;  // keys ka, ka+1, ka+8, ka+9
-        const uint2 va = lds64(vd + ka * kRowBytes + 8 * gq);
-        const uint2 vb = lds64(vd + (ka + 1) * kRowBytes + 8 * gq);
-        const uint2 vc = lds64(vd + (ka + 8) * kRowBytes + 8 * gq);
-        const uint2 ve = lds64(vd + (ka + 9) * kRowBytes + 8 * gq);
-        const uint32_t sab = e4m3x2_to_f16x2(lds8(vs + ka * kRowScales + gq) |
-                                             (lds8(vs + (ka + 1) * kRowScales + gq) << 8));
-        const uint32_t scd = e4m3x2_to_f16x2(lds8(vs + (ka + 8) * kRowScales + gq) |
-                                             (lds8(vs + (ka + 9) * kRowScales + gq) << 8));
-#pragma unroll
-        for (int hw = 0; hw < 2; ++hw) {
-          const uint32_t wa = hw ? va.y : va.x, wb = hw ? vb.y : vb.x;
-          const uint32_t wc = hw ? vc.y : vc.x, we = hw ? ve.y : ve.x;
-          // byte i of lo*: low nibbles of (key a, key b); of hi*: their high nibbles
-          const uint32_t lo_ab = (wa & 0x0F0F0F0Fu) | ((wb & 0x0F0F0F0Fu) << 4);
-          const uint32_t hi_ab = ((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u);
-          const uint32_t lo_ce = (wc & 0x0F0F0F0Fu) | ((we & 0x0F0F0F0Fu) << 4);
-          const uint32_t hi_ce = ((wc >> 4) & 0x0F0F0F0Fu) | (we & 0xF0F0F0F0u);
-          uint32_t la[4], ha[4], lc[4], hc[4];
-          e2m1x8_to_f16x2(lo_ab, la[0], la[1], la[2], la[3]);
-          e2m1x8_to_f16x2(hi_ab, ha[0], ha[1], ha[2], ha[3]);
-          e2m1x8_to_f16x2(lo_ce, lc[0], lc[1], lc[2], lc[3]);
-          e2m1x8_to_f16x2(hi_ce, hc[0], hc[1], hc[2], hc[3]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int mt = hw * 4 + i;  // output dims 16*gq + 2*mt (+1)
-            mma_f16_16816(o[mt], hmul2(la[i], sab), hmul2(ha[i], sab), hmul2(lc[i], scd), hmul2(hc[i], scd), b0,
-                          b1);
+        for (int w = 0; w < kTW; ++w) {
+          const float mw = team_red[w * kRedFloats + kHeadsMax * kDim + h];
+          if (mw != -INFINITY) {
+            const float f = exp2f(mw - M);
+            num += f * team_red[w * kRedFloats + h * kDim + d];
+            den += f * team_red[w * kRedFloats + kHeadsMax * kDim + kHeadsMax + h];
           }
         }
       }
-    }
-    __syncthreads();  // every warp is done with the slots before they are refilled / reused
-  }
-
-  // ---- merge the 4 warps' states in shared memory (aliases the page slots)
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    float v = l_run[e];
-    v += __shfl_xor_sync(0xffffffffu, v, 4);
-    v += __shfl_xor_sync(0xffffffffu, v, 8);
-    v += __shfl_xor_sync(0xffffffffu, v, 16);
-    l_run[e] = v;
-  }
-  float* red_o = reinterpret_cast<float*>(smem);            // [warp][head 8][dim 128]
-  float* red_m = red_o + kAttnWarps * 8 * kDim;             // [warp][8]
-  float* red_l = red_m + kAttnWarps * 8;                    // [warp][8]
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = 16 * gq + 2 * mt;
-    float* base = red_o + warp * 8 * kDim;
-    base[(2 * t4) * kDim + d0] = o[mt][0];
-    base[(2 * t4 + 1) * kDim + d0] = o[mt][1];
-    base[(2 * t4) * kDim + d0 + 1] = o[mt][2];
-    base[(2 * t4 + 1) * kDim + d0 + 1] = o[mt][3];
-  }
-  if (gq == 0) {
-    red_m[warp * 8 + 2 * t4] = m_run[0];
-    red_m[warp * 8 + 2 * t4 + 1] = m_run[1];
-    red_l[warp * 8 + 2 * t4] = l_run[0];
-    red_l[warp * 8 + 2 * t4 + 1] = l_run[1];
-  }
-  __syncthreads();
-  const int d = tid;  // 128 threads = 128 dims
-  for (int h = 0; h < Hg; ++h) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, red_m[w * 8 + h]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kAttnWarps; ++w) {
-        const float mw = red_m[w * 8 + h];
-        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        num += f * red_o[(w * 8 + h) * kDim + d];
-        den += f * red_l[w * 8 + h];
+      if (whole) {
+        write_out(a, ri.head_row0 + h, d, num, den, M);
+      } else {
+        slot_part[h * (kDim + 2) + d] = num;
+        if (d == 0) {
+          slot_part[h * (kDim + 2) + kDim] = M;
+          slot_part[h * (kDim + 2) + kDim + 1] = den;
+        }
       }
     }
-    const int64_t hr = head_row0 + h;
-    if (a.splits == 1) {
-      store_out(a, hr, d, num, den, M);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tb->freed);
+    ++nseg;
+    return true;
+  };
+
+  uint4 qn0 = make_uint4(0u, 0u, 0u, 0u), qn1 = qn0;  // next row's raw FP8 queries
+  int64_t q_row = -1;
+  while (true) {
+    const int slot = consumed % kTSl;
+    if (!mbar_wait_warp(&tb->full[slot], (consumed / kTSl) & 1)) {
+      failed = true;
+      break;
+    }
+    const int64_t row = my_meta[slot].row;
+    const int blk = my_meta[slot].blk;
+    const int page = my_meta[slot].page;
+    if (row != cur_row) {
+      if (cur_row >= 0 && !finalize(cur_row)) {
+        failed = true;
+        break;
+      }
+      if (row >= 0) {
+        ri = row_info(a, row);
+        pos = ri.L - a.q_len + ri.t;
+        if (q_row != row) load_q_raw(a, ri.head_row0, ri.ok, gq, t4, qn0, qn1);
+        q_fragments(qn0, qn1, bq);
+        // prefetch the next row's queries (rows of a range are consecutive)
+        if ((row + 1) * kTopK < x1) {
+          const RowInfo rn = row_info(a, row + 1);
+          load_q_raw(a, rn.head_row0, rn.ok, gq, t4, qn0, qn1);
+          q_row = row + 1;
+        }
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      }
+      cur_row = row;
+    }
+    if (page >= 0)
+      attend_quarter(my_slots + slot * kSlotBytes, wt, blk, ri.r, pos, a.scale_log2, gq, t4, bq, m_run, l_run, o);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tb->empty[slot]);
+    ++consumed;
+    if (row < 0) break;
+    if (wt == 0 && !end_sent) {  // refill the slot just consumed once every warp is done with it
+      if (!mbar_wait_warp(&tb->empty[slot], ((consumed - 1) / kTSl) & 1)) {
+        failed = true;
+        break;
+      }
+      produce_one();
+    }
+  }
+
+  if (failed && lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
+  // the producer drains its copies still in flight (only after a timeout; bounded)
+  if (wt == 0)
+    for (int k = consumed; k < produced; ++k) mbar_wait(&tb->full[k % kTSl], (k / kTSl) & 1);
+}
+
+// Rows cut by team-range boundaries: combine the partial states the teams left.  One CTA per
+// boundary (the first boundary inside a row owns the row), one thread per (head, dim), one
+// online pass over the row's segments so that all their loads are in flight together.
+__global__ void __launch_bounds__(kHeadsMax * kDim) merge_kernel(const AttnArgs a, int NT) {
+  grid_dependency_wait();
+  const int k = blockIdx.x + 1;  // boundary between ranges k-1 and k
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
+  const int64_t E = rows * kTopK;
+  const int64_t xb = range_lo(E, k, NT);
+  if (xb % kTopK == 0 || xb >= E) return;  // not inside a row
+  const int64_t R = xb / kTopK;
+  if (range_lo(E, k - 1, NT) > R * kTopK) return;  // an earlier boundary inside this row owns it
+  const int ca = owner_of(E, R * kTopK, NT), cbk = owner_of(E, R * kTopK + kTopK - 1, NT);
+  const int h = threadIdx.x / kDim, d = threadIdx.x % kDim;
+  if (h >= a.heads_per_group) return;
+  float M = -INFINITY, num = 0.f, den = 0.f;
+#pragma unroll 4
+  for (int cc = ca; cc <= cbk; ++cc) {
+    const int64_t lo = range_lo(E, cc, NT), hi = range_lo(E, cc + 1, NT);
+    if (lo >= hi) continue;  // empty range
+    const float* part =
+        a.partial + static_cast<int64_t>(2 * cc + ((lo / kTopK) == R ? 0 : 1)) * kSlotFloats + h * (kDim + 2);
+    const float ms = __ldcg(part + kDim), ls = __ldcg(part + kDim + 1), os = __ldcg(part + d);
+    if (ms == -INFINITY) continue;
+    if (ms > M) {
+      const float f = (M == -INFINITY) ? 0.f : exp2f(M - ms);
+      num = num * f + os;
+      den = den * f + ls;
+      M = ms;
     } else {
-      float* part = a.partial + (hr * a.splits + split) * kPartialStride;
-      part[d] = num;
-      if (d == 0) {
-        part[kDim] = M;
-        part[kDim + 1] = den;
-      }
+      const float f = exp2f(ms - M);
+      num += f * os;
+      den += f * ls;
     }
   }
+  const RowInfo ri = row_info(a, R);
+  write_out(a, ri.head_row0 + h, d, num, den, M);
 }
 
-// Combine the splits of one head row: 128 threads, one per dim.
-__global__ void __launch_bounds__(kDim) merge_kernel(const AttnArgs a) {
-  const int64_t hr = blockIdx.x;
-  const int d = threadIdx.x;
-  const float* part = a.partial + hr * a.splits * kPartialStride;
-  float M = -INFINITY;
-  for (int s = 0; s < a.splits; ++s) M = fmaxf(M, part[s * kPartialStride + kDim]);
-  float num = 0.f, den = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < a.splits; ++s) {
-      const float ms = part[s * kPartialStride + kDim];
-      const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      num += f * part[s * kPartialStride + d];
-      den += f * part[s * kPartialStride + kDim + 1];
-    }
-  }
-  store_out(a, hr, d, num, den, M);
+size_t attn_partial_bytes() {
+  return static_cast<size_t>(2) * kAttnMaxCtas * kTeams * kSlotFloats * sizeof(float);
 }
 
-cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
-  const int64_t bt = static_cast<int64_t>(a.batch) * a.q_len;
-  if (bt == 0) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(kAttnSlots) * kSlotBytes + kAttnSlots * sizeof(uint64_t);
+cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
+  if (rows == 0) return cudaSuccess;
+  const int NC = num_sms < kAttnMaxCtas ? num_sms : kAttnMaxCtas;
+  const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.splits, a.groups, static_cast<unsigned>(bt));
-  attention_kernel<<<grid, kAttnWarps * 32, smem, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.splits == 1) return e;
-  merge_kernel<<<static_cast<unsigned>(bt * a.groups * a.heads_per_group), kDim, 0, s>>>(a);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(NC);
+  cfg.blockDim = dim3(kAW * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attention_kernel, a);
+  if (e != cudaSuccess) return e;
+  const int NT = NC * kTeams;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(NT - 1);
+  mcfg.blockDim = dim3(kDim * a.heads_per_group);
+  mcfg.stream = s;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&mcfg, merge_kernel, a, NT);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -34,7 +34,7 @@
 
 namespace msa {
 
-constexpr int kIdxWarps = 8;
+constexpr int kIdxWarps = 12;
 constexpr int kIdxStages = 2;
 constexpr int kStageBytes = kPageData + kPageScale;  // 9216
 
@@ -48,13 +48,73 @@ __device__ __forceinline__ int find_seq(const int32_t* prefix, int batch, int64_
   return lo;
 }
 
+// Walks the pages of one warp's unit range in order: unit u of sequence b covers page
+// (u - prefix[b]) / nchunks.  Monotone, so the sequence index only ever moves forward.
+struct PageCursor {
+  int64_t u;      // first unit of the current page (within the warp's range)
+  int b;          // its sequence
+  int64_t b_end;  // prefix[b + 1]
+  __device__ void init(const int32_t* prefix, int batch, int64_t u0, int64_t u1) {
+    u = u0;
+    b = (u0 < u1) ? find_seq(prefix, batch, u0) : 0;
+    b_end = prefix[b + 1];
+  }
+  __device__ void settle(const int32_t* prefix) {
+    while (u >= b_end) {
+      ++b;
+      b_end = prefix[b + 1];
+    }
+  }
+};
+
+// Scores of one 16-key tile against NT n-tiles of 8 query rows.  Keys are the M dimension
+// (rows g and g+8 of the tile), query rows the N dimension.  Two accumulators per n-tile
+// (even / odd k-steps) halve the MMA dependency chain; the caller adds them.
+template <int NT>
+__device__ __forceinline__ void score_tile(const uint8_t* st, int r0, int t4, const uint32_t (&bq)[NT][8][2],
+                                           float (&acc)[NT][2][4]) {
+  const int r1 = r0 + 8;
+  const uint4 d0 = lds128(st + r0 * kRowBytes + 16 * t4);
+  const uint4 d1 = lds128(st + r1 * kRowBytes + 16 * t4);
+  const uint32_t s0 = lds16(st + kPageData + r0 * kRowScales + 2 * t4);
+  const uint32_t s1 = lds16(st + kPageData + r1 * kRowScales + 2 * t4);
+  const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
+  const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
+  const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
+  const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+    e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
+    e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
+    const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
+    x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
+    y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_f16_16816(acc[nt][0], x0, y0, x1, y1, bq[nt][2 * w][0], bq[nt][2 * w][1]);
+      mma_f16_16816(acc[nt][1], x2, y2, x3, y3, bq[nt][2 * w + 1][0], bq[nt][2 * w + 1][1]);
+    }
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const IndexerArgs a) {
+  // key tiles processed together: enough independent MMA chains per warp
+  constexpr int MG = NT == 1 ? 4 : (NT == 2 ? 2 : 1);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kIdxWarps * kIdxStages * kStageBytes);
   int32_t* prefix = reinterpret_cast<int32_t*>(bars + kIdxWarps * kIdxStages);
   __shared__ int32_t warp_tot[kIdxWarps];
+
+  // launched as a programmatic dependent of the previous kernel on the stream: wait for it
+  // (and its memory) before touching global memory
+  grid_dependency_wait();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -109,19 +169,29 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
   uint8_t* my_stages = stages + warp * kIdxStages * kStageBytes;
   uint64_t* my_bars = bars + warp * kIdxStages;
 
-  // ---- issue side: page-granular cursor running ahead of the consumer
-  int64_t ucur_issue = u0;
+  // ---- issue side: a cursor one page ahead of the copies, whose block-table entry is
+  // loaded one issue early so that its latency hides behind a page of compute
+  PageCursor ic;
+  ic.init(prefix, a.batch, u0, u1);
+  int next_page = -1;
+  auto lookup_next = [&]() {
+    if (ic.u < u1) {
+      ic.settle(prefix);
+      const int n = static_cast<int>((ic.u - prefix[ic.b]) / nchunks);
+      next_page = __ldg(a.block_table + static_cast<int64_t>(ic.b) * a.max_blocks + n);
+    }
+  };
+  uint32_t valid_bits = 0;  // bit s: the page in stage s has a valid id
   auto issue_next = [&](int stage) {
-    // all lanes evaluate (uniform); lane 0 issues
-    const int b = find_seq(prefix, a.batch, ucur_issue);
-    const int64_t local = ucur_issue - prefix[b];
-    const int n = static_cast<int>(local / nchunks);
-    const int64_t end = prefix[b] + static_cast<int64_t>(n + 1) * nchunks;
-    ucur_issue = end < u1 ? end : u1;
-    const int page = a.block_table[static_cast<int64_t>(b) * a.max_blocks + n];
+    const int n = static_cast<int>((ic.u - prefix[ic.b]) / nchunks);
+    const int64_t end = prefix[ic.b] + static_cast<int64_t>(n + 1) * nchunks;
+    const int page = next_page;
+    ic.u = end < u1 ? end : u1;
+    const bool ok = page >= 0 && page < a.num_pages;
+    valid_bits = ok ? (valid_bits | (1u << stage)) : (valid_bits & ~(1u << stage));
     if (lane == 0) {
       uint64_t* bar = &my_bars[stage];
-      if (page >= 0 && page < a.num_pages) {
+      if (ok) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, kStageBytes);
         uint8_t* dst = my_stages + stage * kStageBytes;
@@ -132,31 +202,34 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
         mbar_arrive(bar);
       }
     }
+    lookup_next();
   };
 
+  lookup_next();
   int issued = 0;
-  for (int s = 0; s < kIdxStages && ucur_issue < u1; ++s, ++issued) issue_next(s);
+  for (int s = 0; s < kIdxStages && ic.u < u1; ++s, ++issued) issue_next(s);
 
-  // ---- consumer state
-  uint32_t bq[NT][8][2];  // B fragments (index queries), one chunk of one sequence
-  int cur_b = -1, cur_c = -1;
-  int64_t ucur = u0;
+  // ---- consumer
+  uint32_t bq[NT][8][2];  // B fragments (index queries) of one chunk of one sequence
+  int cur_b = -1, cur_c = -1, L = 0;
+  PageCursor cc;
+  cc.init(prefix, a.batch, u0, u1);
   int consumed = 0;
   bool timed_out = false;
 
-  while (ucur < u1) {
-    const int b = find_seq(prefix, a.batch, ucur);
-    const int64_t local = ucur - prefix[b];
+  while (cc.u < u1) {
+    cc.settle(prefix);
+    const int b = cc.b;
+    const int64_t local = cc.u - prefix[b];
     const int n = static_cast<int>(local / nchunks);
     const int c_lo = static_cast<int>(local - static_cast<int64_t>(n) * nchunks);
     const int64_t end = prefix[b] + static_cast<int64_t>(n + 1) * nchunks;
     const int64_t uend = end < u1 ? end : u1;
-    const int c_hi = c_lo + static_cast<int>(uend - ucur);
+    const int c_hi = c_lo + static_cast<int>(uend - cc.u);
     const int stage = consumed % kIdxStages;
     const uint32_t parity = (consumed / kIdxStages) & 1;
-    const int page = a.block_table[static_cast<int64_t>(b) * a.max_blocks + n];
-    const bool page_ok = page >= 0 && page < a.num_pages;
-    const int L = a.seq_lens[b];
+    const bool page_ok = (valid_bits >> stage) & 1u;
+    if (b != cur_b) L = a.seq_lens[b];
 
     if (!mbar_wait_warp(&my_bars[stage], parity)) {
       timed_out = true;
@@ -208,48 +281,33 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
           }
         const bool need_mask = (n + 1) * kBlock - 1 > pos_min;
 
-#pragma unroll 2
-        for (int mt = 0; mt < 8; ++mt) {
-          const int r0 = mt * 16 + g, r1 = r0 + 8;
-          const uint4 d0 = lds128(st + r0 * kRowBytes + 16 * t4);
-          const uint4 d1 = lds128(st + r1 * kRowBytes + 16 * t4);
-          const uint32_t s0 = lds16(st + kPageData + r0 * kRowScales + 2 * t4);
-          const uint32_t s1 = lds16(st + kPageData + r1 * kRowScales + 2 * t4);
-          const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
-          const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
-          const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
-          const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
-          float acc[NT][4];
+#pragma unroll 1
+        for (int mt0 = 0; mt0 < 8; mt0 += MG) {
+          float acc[MG][NT][2][4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+          for (int k = 0; k < MG; ++k) score_tile<NT>(st, (mt0 + k) * 16 + g, t4, bq, acc[k]);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-            e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
-            e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
-            const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
-            x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
-            y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
+          for (int k = 0; k < MG; ++k) {
+            float v[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) v[nt][e] = acc[k][nt][0][e] + acc[k][nt][1][e];
+            if (need_mask) {
+              const int j0 = n * kBlock + (mt0 + k) * 16 + g, j1 = j0 + 8;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (j0 > posc[nt][0]) v[nt][0] = -INFINITY;
+                if (j0 > posc[nt][1]) v[nt][1] = -INFINITY;
+                if (j1 > posc[nt][0]) v[nt][2] = -INFINITY;
+                if (j1 > posc[nt][1]) v[nt][3] = -INFINITY;
+              }
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              mma_f16_16816(acc[nt], x0, y0, x1, y1, bq[nt][2 * w][0], bq[nt][2 * w][1]);
-              mma_f16_16816(acc[nt], x2, y2, x3, y3, bq[nt][2 * w + 1][0], bq[nt][2 * w + 1][1]);
+              mx[nt][0] = fmaxf(mx[nt][0], fmaxf(v[nt][0], v[nt][2]));
+              mx[nt][1] = fmaxf(mx[nt][1], fmaxf(v[nt][1], v[nt][3]));
             }
-          }
-          if (need_mask) {
-            const int j0 = n * kBlock + r0, j1 = j0 + 8;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              if (j0 > posc[nt][0]) acc[nt][0] = -INFINITY;
-              if (j0 > posc[nt][1]) acc[nt][1] = -INFINITY;
-              if (j1 > posc[nt][0]) acc[nt][2] = -INFINITY;
-              if (j1 > posc[nt][1]) acc[nt][3] = -INFINITY;
-            }
-          }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mx[nt][0] = fmaxf(mx[nt][0], fmaxf(acc[nt][0], acc[nt][2]));
-            mx[nt][1] = fmaxf(mx[nt][1], fmaxf(acc[nt][1], acc[nt][3]));
           }
         }
 #pragma unroll
@@ -278,8 +336,8 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
     }
     __syncwarp();
     ++consumed;
-    ucur = uend;
-    if (ucur_issue < u1) {
+    cc.u = uend;
+    if (ic.u < u1) {
       issue_next(issued % kIdxStages);
       ++issued;
     }
@@ -308,7 +366,18 @@ static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) 
   cudaError_t e = cudaFuncSetAttribute(indexer_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  indexer_kernel<NT><<<num_sms, kIdxWarps * 32, smem, s>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kIdxWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, indexer_kernel<NT>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

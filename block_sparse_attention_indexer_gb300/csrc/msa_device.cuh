@@ -92,6 +92,12 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return d;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Kernels launched with programmatic stream serialization may start while the previous
+// kernel on the stream is still finishing; this waits until it has completed and its
+// memory is visible (a no-op when there is no such kernel).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier + bulk copy
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -25,6 +25,7 @@ struct SelectArgs {
   const int32_t* seq_lens;
   int32_t batch, max_blocks, q_len, groups;
   int32_t* selection;          // [B][T][G][16]
+  int32_t row_cap;             // candidates per row staged in shared memory (set by the launcher)
 };
 
 struct AttnArgs {
@@ -40,8 +41,7 @@ struct AttnArgs {
   const int32_t* selection;    // [B][T][G][16]
   uint16_t* out;               // [B][T][H][128] bf16
   float* lse;                  // [B][T][H] or null
-  float* partial;              // [B][T][H][splits][130] when splits > 1
-  int32_t splits;
+  float* partial;              // attn_partial_bytes(): two partial-state slots per CTA
   float scale_log2;            // softmax_scale * log2(e)
   uint32_t* err;
 };
@@ -62,18 +62,17 @@ cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_quantize(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
 cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
-cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s);
+
+// Upper bound of the attention grid (one CTA per SM); the partial-state area is sized for it.
+constexpr int kAttnMaxCtas = 160;
+// Bytes of the attention partial-state area (independent of the batch).
+size_t attn_partial_bytes();
 
 // Kernel-side limits the host validates against.
-constexpr int kMaxBatchSmem = 4096;   // sequences per call (the indexer keeps a prefix table in smem)
+constexpr int kMaxBatchSmem = 2048;   // sequences per call (the indexer keeps a prefix table in smem)
 constexpr int kSelTopK = 16;          // selection width the kernels are built for
 
-inline int attn_splits(int64_t rows) {
-  // split-K factor over the 16 selected blocks: enough CTAs to fill the GPU several times
-  int64_t want = (1024 + rows - 1) / rows;
-  int s = 1;
-  while (s < 16 && s < want) s <<= 1;
-  return s;
-}
+
 
 }  // namespace msa

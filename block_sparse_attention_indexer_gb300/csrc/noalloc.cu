@@ -54,7 +54,8 @@ extern "C" msa_status_t msa_sparse_attn_decode_noalloc(const msa_config_t* cfg, 
   void* scratch = nullptr;
   msa_status_t st = noalloc_scratch(&scratch);
   if (st != MSA_OK) return st;
-  // the error word starts at zero on every call; the partial states are fully overwritten
+  // the error word starts at zero on every call; the partial states are written before they
+  // are read
   if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MSA_ERR_CUDA;
   return msa_sparse_attn_decode(cfg, cache, batch, q, selection, out, lse, scratch, kNoAllocScratchBytes, stream);

@@ -10,14 +10,15 @@
 //
 // One warp per (sequence, query token, KV group) row.  Every candidate n < r gets the
 // 64-bit key  order(score) << 32 | (0xffffffff - n)  (all keys distinct, larger = better).
-//   1. each lane takes the max key of its strided share; the 15th largest lane maximum
-//      is a lower bound of the 15th largest key overall (15 lanes each hold a key >= it);
-//   2. keys >= that bound (at least 15, typically a few dozen) are compacted to shared
-//      memory;
-//   3. 15 rounds of warp arg-max over the survivors pick the winners; a lane-parallel rank
-//      sort writes them ascending with r.
-// If step 2 overflows its buffer (adversarial score layouts) step 3 runs over the whole
-// row instead, with the same result.
+//   1. each lane takes the largest score order (32-bit, without the index) of its strided
+//      share; the 15th largest lane maximum is a lower bound of the 15th best candidate
+//      (15 lanes each hold one at least that large);
+//   2. candidates at or above that bound (at least 15, typically a few dozen) are compacted
+//      to shared memory as their exact 64-bit keys;
+//   3. if at most 32 survive (the usual case) one bitonic sort across the warp ranks them;
+//      otherwise 15 rounds of warp arg-max pick the winners, over the compacted survivors
+//      or, if they overflowed the buffer (adversarial score layouts), over the whole row;
+//   4. a bitonic sort of the 16 ids writes them ascending.
 #include "msa_device.cuh"
 #include "msa_kernels.h"
 
@@ -26,9 +27,6 @@ namespace msa {
 constexpr int kSelWarps = 4;
 constexpr int kSelCap = 512;
 
-__device__ __forceinline__ uint64_t cand_key(float s, int n) {
-  return (static_cast<uint64_t>(score_order(s)) << 32) | static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(n));
-}
 
 __device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
   uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v), src);
@@ -51,9 +49,58 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
   return v;
 }
 
+// Bitonic sort of one 64-bit key per lane across the warp, descending (lane 0 largest).
+__device__ __forceinline__ uint64_t warp_sort_desc_u64(uint64_t v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t o = shfl_xor_u64(v, stride);
+      const bool desc = ((lane & size) == 0);   // direction of this bitonic run
+      const bool lower = ((lane & stride) == 0);
+      v = (lower == desc) ? (o > v ? o : v) : (o < v ? o : v);
+    }
+  }
+  return v;
+}
+
+// The same for one int per lane, ascending.
+__device__ __forceinline__ int warp_sort_asc_i32(int v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool asc = ((lane & size) == 0);
+      const bool lower = ((lane & stride) == 0);
+      v = (lower == asc) ? min(o, v) : max(o, v);
+    }
+  }
+  return v;
+}
+
+// Bitonic sort of one 32-bit key per lane, descending (lane 0 largest).
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool desc = ((lane & size) == 0);
+      const bool lower = ((lane & stride) == 0);
+      v = (lower == desc) ? max(o, v) : min(o, v);
+    }
+  }
+  return v;
+}
+
 __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs a) {
+  extern __shared__ __align__(16) uint32_t sord_all[];  // [kSelWarps][row_cap] staged score orders
   __shared__ uint64_t buf[kSelWarps][kSelCap];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // launched as a programmatic dependent of the previous kernel on the stream: wait for it
+  // (and its memory) before touching global memory
+  grid_dependency_wait();
   const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
   if (row >= nrows) return;
@@ -67,87 +114,111 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs
   }
   const int pos = L - a.q_len + t;
   const int r = pos / kBlock;
-  const float* s = a.block_scores + row * a.max_blocks;
   if (r < kTopK) {  // every block 0..r is selected
     if (lane < kTopK) out[lane] = lane <= r ? lane : -1;
     return;
   }
+  const float* s = a.block_scores + row * a.max_blocks;
+  const bool staged = r <= a.row_cap;
+  uint32_t* sord = sord_all + static_cast<int64_t>(warp) * a.row_cap;
 
-  // 1. lane maxima and their 15th largest (bitonic sort across the warp, descending)
-  uint64_t lmax = 0;
-  for (int n = lane; n < r; n += 32) {
-    const uint64_t k = cand_key(s[n], n);
-    lmax = k > lmax ? k : lmax;
-  }
-  uint64_t v = lmax;
+  // 1. score orders of the candidates (32 loads in flight per lane), staged, with the
+  //    lane maxima; the 15th largest lane maximum bounds the winners from below (15 lanes
+  //    each hold a candidate at least that large)
+  uint32_t lmax = 0;
+  for (int n0 = 0; n0 < r; n0 += 32 * 32) {
+    float v[32];
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
+    for (int k = 0; k < 32; ++k) {
+      const int n = n0 + 32 * k + lane;
+      v[k] = n < r ? __ldcg(s + n) : 0.f;
+    }
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const uint64_t o = shfl_xor_u64(v, stride);
-      const bool desc = ((lane & size) == 0);        // direction of this bitonic run
-      const bool lower = ((lane & stride) == 0);
-      const bool keep_max = (lower == desc);
-      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    for (int k = 0; k < 32; ++k) {
+      const int n = n0 + 32 * k + lane;
+      if (n < r) {
+        const uint32_t o = score_order(v[k]);
+        if (staged) sord[n] = o;
+        lmax = max(lmax, o);
+      }
     }
   }
-  const uint64_t bound = shfl_u64(v, kTopK - 2);    // 15th largest lane maximum
+  const uint32_t bound = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lmax, lane), kTopK - 2);
+  __syncwarp();
 
-  // 2. compact keys >= bound
+  // 2. compact the candidates whose order is >= bound (at least 15) as exact 64-bit keys
   uint64_t* cb = buf[warp];
   int count = 0;
   for (int n0 = 0; n0 < r; n0 += 32) {
     const int n = n0 + lane;
-    uint64_t k = 0;
-    bool take = false;
-    if (n < r) {
-      k = cand_key(s[n], n);
-      take = k >= bound;
-    }
+    uint32_t o = 0;
+    if (n < r) o = staged ? sord[n] : score_order(__ldcg(s + n));
+    const bool take = n < r && o >= bound;
     const uint32_t m = __ballot_sync(0xffffffffu, take);
     const int idx = count + __popc(m & ((1u << lane) - 1u));
-    if (take && idx < kSelCap) cb[idx] = k;
+    if (take && idx < kSelCap)
+      cb[idx] = (static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(n));
     count += __popc(m);
   }
   __syncwarp();
-  const bool overflow = count > kSelCap;
 
-  // 3. 15 rounds of arg-max below the previous winner
-  uint64_t prev = ~0ull;
-  int mine = -1;  // lane i (< 15) keeps the i-th winner's block index
-  for (int round = 0; round < kTopK - 1; ++round) {
-    uint64_t best = 0;
-    if (!overflow) {
-      for (int i = lane; i < count; i += 32) {
-        const uint64_t k = cb[i];
-        if (k < prev && k > best) best = k;
+  // 3. the 15 winners
+  int mine = -1;  // lane i (< 15) holds the block of the i-th winner
+  if (count <= 32) {
+    const uint64_t k = lane < count ? cb[lane] : 0ull;
+    const uint64_t sorted = warp_sort_desc_u64(k, lane);
+    if (lane < kTopK - 1) mine = static_cast<int>(0xffffffffu - static_cast<uint32_t>(sorted));
+  } else {
+    const bool overflow = count > kSelCap;
+    uint64_t prev = ~0ull;
+    for (int round = 0; round < kTopK - 1; ++round) {
+      uint64_t best = 0;
+      if (!overflow) {
+        for (int i = lane; i < count; i += 32) {
+          const uint64_t k = cb[i];
+          if (k < prev && k > best) best = k;
+        }
+      } else {
+        for (int n = lane; n < r; n += 32) {
+          const uint32_t o = staged ? sord[n] : score_order(__ldcg(s + n));
+          const uint64_t k = (static_cast<uint64_t>(o) << 32) | (0xffffffffu - static_cast<uint32_t>(n));
+          if (k < prev && k > best) best = k;
+        }
       }
-    } else {
-      for (int n = lane; n < r; n += 32) {
-        const uint64_t k = cand_key(s[n], n);
-        if (k < prev && k > best) best = k;
-      }
+      best = warp_max_u64(best);
+      prev = best;
+      if (lane == round) mine = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best));
     }
-    best = warp_max_u64(best);
-    prev = best;
-    if (lane == round) mine = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best));
   }
   if (lane == kTopK - 1) mine = r;
-  // rank sort of the 16 ids (all distinct)
-  int rank = 0;
-#pragma unroll
-  for (int i = 0; i < kTopK; ++i) {
-    const int other = __shfl_sync(0xffffffffu, mine, i);
-    rank += (other < mine) ? 1 : 0;
-  }
-  if (lane < kTopK) out[rank] = mine;
+  // 4. ascending order of the 16 ids (the other lanes carry INT_MAX)
+  const int sorted_id = warp_sort_asc_i32(lane < kTopK ? mine : 0x7fffffff, lane);
+  if (lane < kTopK) out[lane] = sorted_id;
 }
 
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
+cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
+  SelectArgs a = a0;
   const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
   if (nrows == 0) return cudaSuccess;
-  const int64_t blocks = (nrows + kSelWarps - 1) / kSelWarps;
-  select_kernel<<<static_cast<unsigned>(blocks), kSelWarps * 32, 0, s>>>(a);
+  // stage rows of up to 4096 candidates in shared memory (64 KB for 4 warps); longer rows
+  // are read from L2 on each pass
+  a.row_cap = a.max_blocks < 4096 ? a.max_blocks : 4096;
+  const size_t smem = static_cast<size_t>(kSelWarps) * a.row_cap * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((nrows + kSelWarps - 1) / kSelWarps));
+  cfg.blockDim = dim3(kSelWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, select_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

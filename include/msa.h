@@ -103,7 +103,7 @@ typedef struct {
 typedef struct {
   const int32_t* block_table;  /* [batch][max_blocks] */
   const int32_t* seq_lens;     /* [batch] */
-  int32_t batch;               /* 0..65535 */
+  int32_t batch;               /* 0..2048; batch * q_len <= 65535 */
   int32_t max_blocks;          /* >= 1 */
   int32_t q_len;               /* query tokens per sequence, >= 1 */
 } msa_batch_t;
@@ -164,8 +164,8 @@ msa_status_t msa_indexer_scores(const msa_config_t* cfg, const msa_cache_t* cach
 msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch, const float* block_scores,
                                int32_t* selection, void* stream);
 
-/* Stage 3 -- exact sparse GQA attention over the selected blocks (split-K over the
- * blocks, online softmax, partial merge).  Every head h of group g attends, with
+/* Stage 3 -- exact sparse GQA attention over the selected blocks (the selected pages of all
+ * rows are split evenly across the GPU, online softmax, partial states merged).  Every head h of group g attends, with
  * logits (q . k) * softmax_scale, to the visible keys of selection[b][t][g][:];
  * K/V are dequantised exactly from NVFP4 in the kernel.  out is rounded to bfloat16;
  * lse may be NULL.  workspace: msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...). */
@@ -186,12 +186,12 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
  * must not allocate between decode steps.  The source pages have no counterpart; this is a
  * deployment convenience.
  * Same arguments and results as msa_sparse_attn_decode, minus the workspace: the scratch
- * (split partial states and the device error word) lives in one library-owned device array
- * of 8 MiB, which every GPU that loads the library holds until the process exits.  Nothing
- * is allocated or freed.
- *   - Batches whose msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...) exceeds 8 MiB are rejected
- *     with MSA_ERR_WORKSPACE before anything is launched (the five reference workloads all
- *     fit; 256 rows of (sequence, token, group) with 8 heads need 4.3 MB).
+ * (partial softmax states of rows shared by two CTAs, and the device error word) lives in
+ * one library-owned device array of 8 MiB, which every GPU that loads the library holds
+ * until the process exits.  Nothing is allocated or freed.
+ *   - A call whose msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...) exceeds 8 MiB is rejected
+ *     with MSA_ERR_WORKSPACE before anything is launched.  (This build's attention needs
+ *     4.0 MB whatever the batch, so every valid call fits.)
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *     with that device current); make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents: calls that can

@@ -56,18 +56,18 @@ def test_workspace_sizes(lib):
     b = msa.binding
     cfg = b._Config(4, 8, 128, 128, 128, 16, 0, 1, 0.0)
     f = b._lib.msa_workspace_bytes
-    # 64 sequences x 1 token x 4 groups = 256 rows -> 4 attention splits
+    # 64 sequences x 1 token x 4 groups = 256 rows; the attention's partial-state area is two
+    # slots of 8 heads x 130 floats per team, 3 teams per CTA, up to 160 CTAs, whatever the batch
     bt = b._Batch(1, 1, 64, 1024, 1)
     scores = 256 * 1024 * 4
     sel = 256 * 16 * 4
-    partial = 256 * 8 * 4 * 130 * 4
+    partial = 2 * 160 * 3 * 8 * 130 * 4
     assert f(b.MSA_OP_INDEXER_SCORES, ctypes.byref(cfg), ctypes.byref(bt)) == 256
     assert f(b.MSA_OP_SELECT_BLOCKS, ctypes.byref(cfg), ctypes.byref(bt)) == 0
     assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + partial
     assert f(b.MSA_OP_DECODE, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + scores + sel + partial
-    # 4096 tokens x 4 groups of one sequence: no split, no partial buffer
     bt = b._Batch(1, 1, 1, 544, 4096)
-    assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256
+    assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + partial
     # unsupported configurations report 0
     bad = b._Config(4, 8, 64, 128, 128, 16, 0, 1, 0.0)
     assert f(b.MSA_OP_DECODE, ctypes.byref(bad), ctypes.byref(bt)) == 0
