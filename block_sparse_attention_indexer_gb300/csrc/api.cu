@@ -80,6 +80,12 @@ float scale_log2(const msa_config_t* c) {
 
 msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
+// stage 1: the streaming decode indexer, or its tcgen05 GEMM form for long query chunks
+cudaError_t run_indexer(const IndexerArgs& a, int sms, cudaStream_t s) {
+  if (a.q_len * a.groups >= kPrefillMinRows) return launch_prefill_indexer(a, s);
+  return launch_indexer(a, sms, s);
+}
+
 IndexerArgs indexer_args(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                          const uint8_t* index_q, float* scores, uint32_t* err) {
   IndexerArgs a{};
@@ -200,7 +206,7 @@ msa_status_t msa_indexer_scores(const msa_config_t* cfg, const msa_cache_t* cach
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return MSA_ERR_CUDA;
   IndexerArgs a = indexer_args(cfg, cache, batch, index_q, block_scores, static_cast<uint32_t*>(workspace));
-  return cuda_status(launch_indexer(a, sms, static_cast<cudaStream_t>(stream)));
+  return cuda_status(run_indexer(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch, const float* block_scores,
@@ -256,7 +262,7 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
                      ? selection_out
                      : reinterpret_cast<int32_t*>(ws + kErrBytes + scores_bytes(cfg, batch));
   float* partial = reinterpret_cast<float*>(ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch));
-  cudaError_t e = launch_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
+  cudaError_t e = run_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
   if (e == cudaSuccess) e = launch_select(select_args(cfg, batch, scores, sel), s);
   if (e == cudaSuccess) e = launch_attention(attn_args(cfg, cache, batch, q, sel, out, lse, partial, err), sms, s);
   return cuda_status(e);

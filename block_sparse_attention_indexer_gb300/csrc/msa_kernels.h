@@ -61,6 +61,10 @@ struct QuantArgs {
 cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_quantize(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
 cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s);
+// tcgen05 GEMM form of the indexer for long query chunks (chunked prefill)
+cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s);
+// query rows (token x group) per sequence from which the GEMM form is used
+constexpr int kPrefillMinRows = 64;
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s);
 

@@ -1,0 +1,355 @@
+// Stage 1 for long query chunks (chunked prefill): the indexer as a dense tensor-core GEMM.
+//
+// In prefill the index path scores every candidate KV block for every query token and KV
+// group, reduced per 128-token block with max ("MiniMax M3 x vLLM：百万 token 多模态推理的
+// Day-0 部署", §Prefill 执行 step 2): S[row][n] = max over visible keys j of block n of
+// q_row . k_j with row = (token, group).  With thousands of query rows this is a dense
+// [rows x 128] x [128 x keys] product followed by a max-pool over each 128-key block of
+// its columns, causal (key j visible to token t iff j <= pos(t)).
+//
+// Design (GB300, tcgen05 + TMEM):
+//   * a CTA owns one tile of 128 query rows and a range of 32 key blocks; the query tile is
+//     converted once (FP8 E4M3 -> f16, exact) into a K-major, 128-byte-swizzled shared
+//     tile, the A operand of every MMA of the CTA;
+//   * warp roles: warp 8 streams the raw NVFP4 pages (9 KB) with bulk async copies into a
+//     3-stage ring; warps 4-7 dequantise each page exactly into f16 (cvt e2m1x2 -> f16x2 times
+//     the f16 block scale) in the same swizzled K-major layout (B operand, 2 stages); one
+//     thread of warp 9 issues tcgen05.mma (M = 128 rows, N = 128 keys, K = 16, eight per
+//     block) into one of two 128-column TMEM accumulators; warps 0-3 read the accumulator
+//     back with tcgen05.ld (one TMEM lane quarter each), apply the causal mask and max-pool
+//     the 128 columns into the block's score;
+//   * every hand-off is an mbarrier (tcgen05.commit arrives on the MMA side), every wait is
+//     bounded; key blocks that no row of the tile can see are never loaded.
+#include <cuda_fp16.h>
+
+#include "msa_device.cuh"
+#include "msa_kernels.h"
+
+namespace msa {
+
+constexpr int kPfKb = 32;                 // key blocks per CTA
+constexpr int kPfRawSt = 3;               // raw NVFP4 page stages
+constexpr int kPfKSt = 2;                 // f16 key tile stages
+constexpr int kPfWarps = 10;              // 0-3 epilogue, 4-7 dequant, 8 copies, 9 MMA
+constexpr int kPfRows = 128;              // query rows per CTA (MMA M)
+constexpr int kHalfTile = kPfRows * 128;  // one [128 x 64] f16 K-major SW128 tile: 16 KB
+constexpr int kRawBytes = kPageData + kPageScale;
+
+struct PfShared {
+  uint64_t raw_full[kPfRawSt], raw_empty[kPfRawSt];
+  uint64_t k_full[kPfKSt], k_empty[kPfKSt];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t q_ready;
+  uint32_t tmem_base;
+  int32_t pages[kPfKb];
+};
+
+constexpr size_t kPfSmem = 1024 /* alignment slack */ + 2 * kHalfTile /* Q */ + kPfKSt * 2 * kHalfTile /* K */ +
+                           kPfRawSt * kRawBytes + kPfRows * kPfKb * sizeof(float) + sizeof(PfShared);
+
+// byte offset of 16-byte chunk `chunk` (0..7) of row r in a K-major SW128 tile of 128-byte rows
+__device__ __forceinline__ uint32_t sw128(int r, int chunk) {
+  return static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;                 // leading byte offset (unused when swizzled)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;         // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                 // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// instruction descriptor: f16 A and B (K-major), f32 accumulator, M x N
+__device__ __forceinline__ uint32_t umma_idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const IndexerArgs a, int tiles_per_seq) {
+  extern __shared__ uint8_t smem_raw[];
+  grid_dependency_wait();
+
+  // carve shared memory (tiles 1024-byte aligned for the swizzle)
+  const uint32_t base_u32 = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + ((1024 - (base_u32 & 1023)) & 1023);
+  uint8_t* q_tile = base;                                   // A0 | A1
+  uint8_t* k_tiles = q_tile + 2 * kHalfTile;                // [stage] B0 | B1
+  uint8_t* raw = k_tiles + kPfKSt * 2 * kHalfTile;          // [stage] 9 KB
+  float* sbuf = reinterpret_cast<float*>(raw + kPfRawSt * kRawBytes);  // [128][kPfKb]
+  PfShared* sh = reinterpret_cast<PfShared*>(sbuf + kPfRows * kPfKb);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.q_len, G = a.groups;
+  const int b = blockIdx.y / tiles_per_seq, tile = blockIdx.y % tiles_per_seq;
+  const int rows_seq = T * G;
+  const int row0 = tile * kPfRows;
+  const int nrows = min(kPfRows, rows_seq - row0);
+  const int L = a.seq_lens[b];
+  const bool ok = L > 0 && L >= T && L <= static_cast<int64_t>(a.max_blocks) * kBlock;
+  if (!ok && L != 0 && blockIdx.x == 0 && tile == 0 && tid == 0) flag_error(a.err, MSA_DEVERR_BAD_SEQLEN);
+  const int n0 = blockIdx.x * kPfKb;
+  // blocks some row of this tile can see: n <= r(last token of the tile), n < ceil(L / 128)
+  int nblk = 0;
+  if (ok && nrows > 0) {
+    const int pos_last = L - T + (row0 + nrows - 1) / G;
+    const int nb_eff = min((L + kBlock - 1) / kBlock, pos_last / kBlock + 1);
+    nblk = max(0, min(n0 + kPfKb, nb_eff) - n0);
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < kPfRawSt; ++i) {
+      mbar_init(&sh->raw_full[i], 1);
+      mbar_init(&sh->raw_empty[i], 4);
+    }
+    for (int i = 0; i < kPfKSt; ++i) {
+      mbar_init(&sh->k_full[i], 4);
+      mbar_init(&sh->k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->acc_full[i], 1);
+      mbar_init(&sh->acc_empty[i], 4);
+    }
+    mbar_init(&sh->q_ready, 4);
+    fence_mbar_init();
+  }
+  if (tid < kPfKb) {
+    int page = -1;
+    if (tid < nblk) {
+      page = a.block_table[static_cast<int64_t>(b) * a.max_blocks + n0 + tid];
+      if (page < 0 || page >= a.num_pages) {
+        flag_error(a.err, MSA_DEVERR_BAD_PAGE);
+        page = -1;
+      }
+    }
+    sh->pages[tid] = page;
+  }
+  if (warp == 9 && nblk > 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(&sh->tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  bool failed = false;
+
+  if (nblk > 0) {
+    if (warp == 8) {
+      // ---- raw page producer
+      if (lane == 0) {
+        for (int k = 0; k < nblk && !failed; ++k) {
+          const int s = k % kPfRawSt;
+          if (k >= kPfRawSt && !mbar_wait(&sh->raw_empty[s], ((k / kPfRawSt) - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          const int page = sh->pages[k];
+          if (page >= 0) {
+            uint8_t* dst = raw + s * kRawBytes;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&sh->raw_full[s], kRawBytes);
+            bulk_g2s(dst, a.idx_data + static_cast<int64_t>(page) * kPageData, kPageData, &sh->raw_full[s]);
+            bulk_g2s(dst + kPageData, a.idx_scale + static_cast<int64_t>(page) * kPageScale, kPageScale,
+                     &sh->raw_full[s]);
+          } else {
+            mbar_arrive(&sh->raw_full[s]);
+          }
+        }
+        // after a timeout, wait (bounded) for the copies still in flight before leaving
+        if (failed)
+          for (int k = max(0, nblk - kPfRawSt); k < nblk; ++k) mbar_wait(&sh->raw_full[k % kPfRawSt], (k / kPfRawSt) & 1);
+      }
+    } else if (warp >= 4 && warp < 8) {
+      // ---- dequantisers: the query tile once, then every key page
+      const int dt = tid - 128;
+      for (int item = dt; item < kPfRows * 8; item += 128) {
+        const int r = item >> 3, c = item & 7;  // 16 FP8 query bytes = dims 16c .. 16c+15
+        uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (r < nrows) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+              a.index_q + (static_cast<int64_t>(b) * rows_seq + row0 + r) * kDim + 16 * c));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            h[2 * i] = e4m3x2_to_f16x2(w[i]);
+            h[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+          }
+        }
+        uint8_t* tdst = q_tile + (c < 4 ? 0 : kHalfTile);
+        const int ch = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(tdst + sw128(r, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(tdst + sw128(r, ch + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->q_ready);
+
+      for (int k = 0; k < nblk; ++k) {
+        const int s = k % kPfRawSt, ks = k % kPfKSt;
+        if (!mbar_wait_warp(&sh->raw_full[s], (k / kPfRawSt) & 1) ||
+            (k >= kPfKSt && !mbar_wait_warp(&sh->k_empty[ks], ((k / kPfKSt) - 1) & 1))) {
+          failed = true;
+          break;
+        }
+        const uint8_t* src = raw + s * kRawBytes;
+        uint8_t* kdst = k_tiles + ks * 2 * kHalfTile;
+        for (int item = dt; item < kPfRows * 4; item += 128) {
+          const int r = item >> 2, c = item & 3;  // 16 packed bytes = dims 32c .. 32c+31
+          const uint4 d = lds128(src + r * kRowBytes + 16 * c);
+          const uint32_t sc = lds16(src + kPageData + r * kRowScales + 2 * c);
+          const uint32_t s0 = e4m3_bcast_f16x2(sc, 0), s1 = e4m3_bcast_f16x2(sc, 1);
+          const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+          uint32_t h[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            e2m1x8_to_f16x2(w[i], h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+            const uint32_t sca = i < 2 ? s0 : s1;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[4 * i + j] = hmul2(h[4 * i + j], sca);
+          }
+          uint8_t* tdst = kdst + (c < 2 ? 0 : kHalfTile);
+          const int ch = 4 * (c & 1);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(tdst + sw128(r, ch + q)) =
+                make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sh->k_full[ks]);
+          mbar_arrive(&sh->raw_empty[s]);
+        }
+      }
+    } else if (warp == 9) {
+      // ---- MMA issuer
+      if (lane == 0) {
+        const uint32_t idesc = umma_idesc_f16(kPfRows, kBlock);
+        const uint32_t qa = smem_u32(q_tile);
+        failed = !mbar_wait(&sh->q_ready, 0);
+        for (int k = 0; k < nblk && !failed; ++k) {
+          const int ks = k % kPfKSt, acc = k & 1;
+          if (!mbar_wait(&sh->k_full[ks], (k / kPfKSt) & 1) ||
+              (k >= 2 && !mbar_wait(&sh->acc_empty[acc], ((k / 2) - 1) & 1))) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kb = smem_u32(k_tiles + ks * 2 * kHalfTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >= 4 ? kHalfTile : 0) + (kk & 3) * 32;
+            umma_f16(tmem + acc * kBlock, umma_desc(qa + off), umma_desc(kb + off), idesc, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&sh->k_empty[ks]);
+          umma_commit(&sh->acc_full[acc]);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ---- epilogue (warps 0-3 = TMEM lane quarters 0-3): causal max-pool per block
+      const int r = warp * 32 + lane;
+      const bool row_ok = r < nrows;
+      const int pos = row_ok ? L - T + (row0 + r) / G : -1;
+      for (int k = 0; k < nblk; ++k) {
+        const int acc = k & 1;
+        if (!mbar_wait_warp(&sh->acc_full[acc], (k / 2) & 1)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const int n = n0 + k;
+        const int j0 = n * kBlock;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c0 = 0; c0 < kBlock; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kBlock + c0, v);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (j0 + c0 + 31 <= pos) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j0 + c0 + j <= pos) mx = fmaxf(mx, __uint_as_float(v[j]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
+        sbuf[r * kPfKb + k] = (row_ok && sh->pages[k] >= 0) ? mx : -INFINITY;
+      }
+    }
+  }
+
+  // ---- scores out: the epilogue warps write their 32 rows, a block per lane (coalesced)
+  if (warp < 4) {
+    __syncwarp();
+    const int64_t grow0 = static_cast<int64_t>(b) * rows_seq + row0;
+    for (int i = 0; i < 32; ++i) {
+      const int r = warp * 32 + i;
+      const int n = n0 + lane;
+      if (r < nrows && n < a.max_blocks)
+        a.block_scores[(grow0 + r) * a.max_blocks + n] = lane < nblk ? sbuf[r * kPfKb + lane] : -INFINITY;
+    }
+  }
+  if (failed && lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9 && nblk > 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+}
+
+cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s) {
+  const int rows_seq = a.q_len * a.groups;
+  const int tiles_per_seq = (rows_seq + kPfRows - 1) / kPfRows;
+  const int ranges = (a.max_blocks + kPfKb - 1) / kPfKb;
+  cudaError_t e = cudaFuncSetAttribute(prefill_indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kPfSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ranges, static_cast<unsigned>(a.batch * tiles_per_seq));
+  cfg.blockDim = dim3(kPfWarps * 32);
+  cfg.dynamicSmemBytes = kPfSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, prefill_indexer_kernel, a, tiles_per_seq);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -16,7 +16,9 @@ CASES = [
     ("ragged_t1", [1, 127, 128, 129, 1000, 4096 + 5, 2048, 16 * 128 + 1], 1, 8, True),
     ("spec_t3", [300, 5000, 3 * 128], 3, 4, True),
     ("spec_t8", [8, 2100, 7777], 8, 8, False),
-    ("chunked_t20", [640, 3000], 20, 8, True),
+    ("chunked_t20", [640, 3000], 20, 8, True),               # 80 rows: tcgen05 GEMM indexer
+    ("chunked_t12", [1500, 999, 260], 12, 4, True),          # 48 rows: streaming indexer, 2 chunks
+    ("prefill_t300", [300, 5000 + 77, 40000], 300, 8, True),  # 1,200 rows: several GEMM row tiles
     ("hg4_t1", [4096] * 3, 1, 4, False),
     ("many_rows_t4", [300 + 37 * i for i in range(64)], 4, 8, True),     # 1024 rows: no split
     ("rows256_t2", [2500 + 101 * i for i in range(32)], 2, 8, True),      # 256 rows: 4 splits
