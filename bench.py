@@ -258,10 +258,25 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def step():
-        msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, lse, sel, wsp, stream)
+        # stream=None: the binding uses torch's current stream (the capture stream when graphed)
+        msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, lse, sel, wsp, None)
 
+    def graphed(fn):
+        """fn captured once into a CUDA graph (the launches are capture-safe: no host sync, no
+        allocation, fixed grids); returns the replay callable, or fn itself with --no-graph."""
+        if args.no_graph:
+            return fn
+        fn()  # first call outside capture: per-device set-up (shared-memory limits)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay
+
+    step_run = graphed(step)
     for _ in range(args.warmup):
-        step()
+        step_run()
     torch.cuda.synchronize()
     assert msa.msa_read_device_error(wsp) == 0
 
@@ -278,7 +293,7 @@ def run_ours(args):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record(stream)
-        step()
+        step_run()
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -292,20 +307,21 @@ def run_ours(args):
     ws_att = msa.alloc_workspace(msa.MSA_OP_SPARSE_ATTN, dw.cfg, dw.batch, device=dev)
 
     def timed(fn, n):
+        run = graphed(fn)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         for a, b in ev:
             flush.fill_(1)
             a.record(stream)
-            fn()
+            run()
             b.record(stream)
         torch.cuda.synchronize()
         return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
-    idx_ms = timed(lambda: msa.msa_indexer_scores(dw.cfg, dw.cache, dw.batch, dw.qi, scores, ws_idx, stream),
+    idx_ms = timed(lambda: msa.msa_indexer_scores(dw.cfg, dw.cache, dw.batch, dw.qi, scores, ws_idx, None),
                    args.steps)
-    sel_ms = timed(lambda: msa.msa_select_blocks(dw.cfg, dw.batch, scores, sel, stream), args.steps)
+    sel_ms = timed(lambda: msa.msa_select_blocks(dw.cfg, dw.batch, scores, sel, None), args.steps)
     att_ms = timed(lambda: msa.msa_sparse_attn_decode(dw.cfg, dw.cache, dw.batch, dw.q, sel, out, lse, ws_att,
-                                                      stream), args.steps)
+                                                      None), args.steps)
     clk = clocks.stop()
 
     # ---- end to end through the public API with host buffers (pinned), every step:
@@ -358,11 +374,7 @@ def run_ours(args):
     idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
     att_gbs = kv_bytes / (att_ms / 1e3) / 1e9
     step_gbs = (idx_bytes + kv_bytes) / (ms_step / 1e3) / 1e9
-    splits = 1
-    rows = B * T * 4
-    while splits < 16 and splits < -(-1024 // rows):
-        splits <<= 1
-    launches_per_step = 3 + (1 if splits > 1 else 0)
+    launches_per_step = 4  # indexer, select, attention, partial merge
     traffic = measured_traffic("indexer_kernel", w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
@@ -371,6 +383,7 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": B, "q_len": T, "heads": H, "kv_groups": 4, "head_dim": 128,
                    "index_dim": 128, "top_k": 16, "block": 128, "mean_ctx": float(np.mean(dw.lens)),
                    "tokens_in_cache": int(np.sum(dw.lens)), "l2": "flushed between timed steps (512 MiB write)",
+                   "launch": "eager" if args.no_graph else "cuda graph of one msa_decode call, replayed per step",
                    "parallelism": f"replicas x{ws}"},
         "achieved_hbm_gbs": step_gbs,
         "step_roofline": {"bound": "hbm", "algorithmic_bytes": idx_bytes + kv_bytes, "achieved": step_gbs,
@@ -409,6 +422,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

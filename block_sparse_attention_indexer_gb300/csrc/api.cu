@@ -3,6 +3,8 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
 
 #include "../../include/msa.h"
 #include "msa_kernels.h"
@@ -144,6 +146,21 @@ AttnArgs attn_args(const msa_config_t* cfg, const msa_cache_t* cache, const msa_
 }
 
 }  // namespace
+
+cudaError_t msa::ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t key = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(kernel)) * 131u + static_cast<uint64_t>(dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done[key] = bytes;
+  return e;
+}
 
 extern "C" {
 

@@ -517,8 +517,7 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const int NC = num_sms < kAttnMaxCtas ? num_sms : kAttnMaxCtas;
   const size_t smem = attn_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(attention_kernel), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -67,17 +67,59 @@ struct PageCursor {
   }
 };
 
+// Exclusive prefix over sequences of their work units (pages x query chunks); sequences with
+// an invalid length get none (and flag MSA_DEVERR_BAD_SEQLEN once).  Block-wide scan, ends
+// with __syncthreads.  prefix has batch + 1 entries.
+__device__ __forceinline__ void build_prefix(const IndexerArgs& a, int nchunks, int32_t* prefix, int32_t* warp_tot,
+                                             int nwarps) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.q_len;
+  const int64_t cap = static_cast<int64_t>(a.max_blocks) * kBlock;
+  const int per = (a.batch + blockDim.x - 1) / blockDim.x;
+  const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
+  int local = 0;
+  for (int b = lo; b < hi; ++b) {
+    const int L = a.seq_lens[b];
+    const bool ok = (L >= T) && (L <= cap);
+    if (L != 0 && !ok && blockIdx.x == 0) flag_error(a.err, MSA_DEVERR_BAD_SEQLEN);
+    local += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  int run = base + incl - local;
+  for (int b = lo; b < hi; ++b) {
+    prefix[b] = run;
+    const int L = a.seq_lens[b];
+    const bool ok = (L >= T) && (L <= cap);
+    run += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
+  }
+  if (tid == blockDim.x - 1) {
+    int tot = 0;
+    for (int w = 0; w < nwarps; ++w) tot += warp_tot[w];
+    prefix[a.batch] = tot;
+  }
+  __syncthreads();
+}
+
 // Scores of one 16-key tile against NT n-tiles of 8 query rows.  Keys are the M dimension
 // (rows g and g+8 of the tile), query rows the N dimension.  Two accumulators per n-tile
 // (even / odd k-steps) halve the MMA dependency chain; the caller adds them.
 template <int NT>
-__device__ __forceinline__ void score_tile(const uint8_t* st, int r0, int t4, const uint32_t (&bq)[NT][8][2],
-                                           float (&acc)[NT][2][4]) {
+__device__ __forceinline__ void score_tile(const uint8_t* st, const uint8_t* ss, int r0, int t4,
+                                           const uint32_t (&bq)[NT][8][2], float (&acc)[NT][2][4]) {
   const int r1 = r0 + 8;
   const uint4 d0 = lds128(st + r0 * kRowBytes + 16 * t4);
   const uint4 d1 = lds128(st + r1 * kRowBytes + 16 * t4);
-  const uint32_t s0 = lds16(st + kPageData + r0 * kRowScales + 2 * t4);
-  const uint32_t s1 = lds16(st + kPageData + r1 * kRowScales + 2 * t4);
+  const uint32_t s0 = lds16(ss + r0 * kRowScales + 2 * t4);
+  const uint32_t s1 = lds16(ss + r1 * kRowScales + 2 * t4);
   const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
   const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
   const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
@@ -120,42 +162,8 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
   const int g = lane >> 2, t4 = lane & 3;
   const int T = a.q_len, G = a.groups, TC = a.chunk_tokens;
   const int nchunks = (T + TC - 1) / TC;
-  const int64_t cap = static_cast<int64_t>(a.max_blocks) * kBlock;
 
-  // ---- units per sequence and their exclusive prefix (block-wide scan)
-  {
-    const int per = (a.batch + blockDim.x - 1) / blockDim.x;
-    const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
-    int local = 0;
-    for (int b = lo; b < hi; ++b) {
-      const int L = a.seq_lens[b];
-      const bool ok = (L >= T) && (L <= cap);
-      if (L != 0 && !ok && blockIdx.x == 0) flag_error(a.err, MSA_DEVERR_BAD_SEQLEN);
-      local += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += warp_tot[w];
-    int run = base + incl - local;
-    for (int b = lo; b < hi; ++b) {
-      prefix[b] = run;
-      const int L = a.seq_lens[b];
-      const bool ok = (L >= T) && (L <= cap);
-      run += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
-    }
-    if (tid == blockDim.x - 1) {
-      int tot = 0;
-      for (int w = 0; w < kIdxWarps; ++w) tot += warp_tot[w];
-      prefix[a.batch] = tot;
-    }
-  }
+  build_prefix(a, nchunks, prefix, warp_tot, kIdxWarps);
   if (lane == 0)
     for (int s = 0; s < kIdxStages; ++s) mbar_init(&bars[warp * kIdxStages + s], 1);
   fence_mbar_init();
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
         for (int mt0 = 0; mt0 < 8; mt0 += MG) {
           float acc[MG][NT][2][4];
 #pragma unroll
-          for (int k = 0; k < MG; ++k) score_tile<NT>(st, (mt0 + k) * 16 + g, t4, bq, acc[k]);
+          for (int k = 0; k < MG; ++k) score_tile<NT>(st, st + kPageData, (mt0 + k) * 16 + g, t4, bq, acc[k]);
 #pragma unroll
           for (int k = 0; k < MG; ++k) {
             float v[NT][4];
@@ -359,12 +367,225 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Variant for at most 8 query rows per sequence (T x G <= 8, one n-tile, one query chunk):
+// 16 warps per SM, each streaming half pages (64 keys: 4 KB of E2M1 + 512 B of scales)
+// through a 3-stage ring; the block max combines the two halves in registers.  Twice the
+// warps of the general kernel in the same shared memory, for more latency hiding.
+constexpr int kHWarps = 16;
+constexpr int kHStages = 3;
+constexpr int kHalfData = kPageData / 2;    // 4096
+constexpr int kHalfScale = kPageScale / 2;  // 512
+constexpr int kHalfBytes = kHalfData + kHalfScale;
+
+__global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const IndexerArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kHWarps * kHStages * kHalfBytes);
+  int32_t* prefix = reinterpret_cast<int32_t*>(bars + kHWarps * kHStages);
+  __shared__ int32_t warp_tot[kHWarps];
+
+  grid_dependency_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int T = a.q_len, G = a.groups;
+  const int rows = T * G;  // <= 8
+
+  build_prefix(a, 1, prefix, warp_tot, kHWarps);
+  if (lane == 0)
+    for (int s = 0; s < kHStages; ++s) mbar_init(&bars[warp * kHStages + s], 1);
+  fence_mbar_init();
+  __syncthreads();
+
+  const int64_t total = prefix[a.batch];
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kHWarps;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kHWarps + warp;
+  const int64_t u0 = total * gw / nwarps, u1 = total * (gw + 1) / nwarps;
+  uint8_t* my_stages = stages + warp * kHStages * kHalfBytes;
+  uint64_t* my_bars = bars + warp * kHStages;
+
+  // ---- issue side: half pages in order; the next page's block-table entry is loaded a page early
+  PageCursor ic;
+  ic.init(prefix, a.batch, u0, u1);
+  int next_page = -1, cur_page = -1, ihalf = 0;
+  auto lookup_next = [&]() {
+    if (ic.u < u1) {
+      ic.settle(prefix);
+      next_page = __ldg(a.block_table + static_cast<int64_t>(ic.b) * a.max_blocks + (ic.u - prefix[ic.b]));
+    }
+  };
+  uint32_t valid_bits = 0;
+  auto issue_next = [&](int stage) {
+    if (ihalf == 0) {
+      cur_page = next_page;
+      ++ic.u;
+      lookup_next();
+    }
+    const int page = cur_page;
+    const bool ok = page >= 0 && page < a.num_pages;
+    valid_bits = ok ? (valid_bits | (1u << stage)) : (valid_bits & ~(1u << stage));
+    if (lane == 0) {
+      uint64_t* bar = &my_bars[stage];
+      if (ok) {
+        uint8_t* dst = my_stages + stage * kHalfBytes;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, kHalfBytes);
+        bulk_g2s(dst, a.idx_data + static_cast<int64_t>(page) * kPageData + ihalf * kHalfData, kHalfData, bar);
+        bulk_g2s(dst + kHalfData, a.idx_scale + static_cast<int64_t>(page) * kPageScale + ihalf * kHalfScale,
+                 kHalfScale, bar);
+      } else {
+        if (ihalf == 0) flag_error(a.err, MSA_DEVERR_BAD_PAGE);
+        mbar_arrive(bar);
+      }
+    }
+    ihalf ^= 1;
+  };
+  const int64_t nhalves = 2 * (u1 - u0);
+  int64_t issued = 0;
+  if (u0 < u1) {
+    lookup_next();
+    for (; issued < kHStages && issued < nhalves; ++issued) issue_next(static_cast<int>(issued % kHStages));
+  }
+
+  // ---- consumer
+  uint32_t bq[1][8][2];
+  int cur_b = -1, L = 0, posc[2] = {-1, -1};
+  PageCursor cc;
+  cc.init(prefix, a.batch, u0, u1);
+  int64_t consumed = 0;
+  bool timed_out = false;
+  for (int64_t u = u0; u < u1 && !timed_out; ++u) {
+    cc.u = u;
+    cc.settle(prefix);
+    const int b = cc.b;
+    const int n = static_cast<int>(u - prefix[b]);
+    if (b != cur_b) {
+      cur_b = b;
+      L = a.seq_lens[b];
+      const int r = g;  // n-tile row of this lane's B fragment
+      if (r < rows) {
+        const int tq = r / G, gq = r % G;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.index_q + ((static_cast<int64_t>(b) * T + tq) * G + gq) * kDim + 32 * t4);
+        const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          bq[0][s][0] = e4m3x2_to_f16x2(w[s]);
+          bq[0][s][1] = e4m3x2_to_f16x2(w[s] >> 16);
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) bq[0][s][0] = bq[0][s][1] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = 2 * t4 + e;
+        posc[e] = col < rows ? (L - T + col / G) : -1;
+      }
+    }
+    const int pos_min = L - T;
+    const bool need_mask = (n + 1) * kBlock - 1 > pos_min;
+    float mx[2] = {-INFINITY, -INFINITY};
+    bool page_ok = true;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const int stage = static_cast<int>(consumed % kHStages);
+      if (!mbar_wait_warp(&my_bars[stage], static_cast<uint32_t>((consumed / kHStages) & 1))) {
+        timed_out = true;
+        break;
+      }
+      page_ok = page_ok && ((valid_bits >> stage) & 1u);
+      const uint8_t* st = my_stages + stage * kHalfBytes;
+      if (page_ok) {
+        float acc[4][1][2][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) score_tile<1>(st, st + kHalfData, k * 16 + g, t4, bq, acc[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = acc[k][0][0][e] + acc[k][0][1][e];
+          if (need_mask) {
+            const int j0 = n * kBlock + h * 64 + k * 16 + g, j1 = j0 + 8;
+            if (j0 > posc[0]) v[0] = -INFINITY;
+            if (j0 > posc[1]) v[1] = -INFINITY;
+            if (j1 > posc[0]) v[2] = -INFINITY;
+            if (j1 > posc[1]) v[3] = -INFINITY;
+          }
+          mx[0] = fmaxf(mx[0], fmaxf(v[0], v[2]));
+          mx[1] = fmaxf(mx[1], fmaxf(v[1], v[3]));
+        }
+      }
+      __syncwarp();
+      ++consumed;
+      if (issued < nhalves) {
+        issue_next(static_cast<int>(issued % kHStages));
+        ++issued;
+      }
+    }
+    if (timed_out) break;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = page_ok ? mx[e] : -INFINITY;
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      mx[e] = v;
+    }
+    if (g == 0) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = 2 * t4 + e;
+        if (col < rows) {
+          const int tq = col / G, gq = col % G;
+          a.block_scores[((static_cast<int64_t>(b) * T + tq) * G + gq) * a.max_blocks + n] = mx[e];
+        }
+      }
+    }
+  }
+
+  if (timed_out) {
+    if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
+    for (int64_t k = consumed; k < issued; ++k)
+      mbar_wait(&my_bars[k % kHStages], static_cast<uint32_t>((k / kHStages) & 1));
+  }
+
+  // ---- -inf for blocks past each sequence's end (and whole rows of skipped sequences)
+  const int64_t nrows = static_cast<int64_t>(a.batch) * rows;
+  for (int64_t row = gw; row < nrows; row += nwarps) {
+    const int b = static_cast<int>(row / rows);
+    const int nb = prefix[b + 1] - prefix[b];
+    float* dst = a.block_scores + row * a.max_blocks;
+    for (int n = nb + lane; n < a.max_blocks; n += 32) dst[n] = -INFINITY;
+  }
+}
+
+static cudaError_t launch_half(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(kHWarps) * kHStages * kHalfBytes + kHWarps * kHStages * sizeof(uint64_t) +
+                      (a.batch + 1) * sizeof(int32_t);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(indexer_half_kernel), smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kHWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, indexer_half_kernel, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int NT>
 static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(kIdxWarps) * kIdxStages * kStageBytes +
                       kIdxWarps * kIdxStages * sizeof(uint64_t) + (a.batch + 1) * sizeof(int32_t);
-  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(indexer_kernel<NT>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
@@ -383,6 +604,7 @@ static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) 
 
 cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s) {
   const int rows = a.chunk_tokens * a.groups;
+  if (a.q_len * a.groups <= 8) return launch_half(a, num_sms, s);
   switch ((rows + 7) / 8) {
     case 1: return launch_nt<1>(a, num_sms, s);
     case 2: return launch_nt<2>(a, num_sms, s);

@@ -57,6 +57,10 @@ struct QuantArgs {
   int32_t block_size;
 };
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` the first time a larger size is
+// needed on the current device (later calls are a lookup, so launches stay cheap).
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
 // Launchers return cudaGetLastError() after enqueueing.
 cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_quantize(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
@@ -74,7 +78,7 @@ constexpr int kAttnMaxCtas = 160;
 size_t attn_partial_bytes();
 
 // Kernel-side limits the host validates against.
-constexpr int kMaxBatchSmem = 2048;   // sequences per call (the indexer keeps a prefix table in smem)
+constexpr int kMaxBatchSmem = 2048;   // sequences per call (the indexers keep a prefix table in smem)
 constexpr int kSelTopK = 16;          // selection width the kernels are built for
 
 

@@ -334,8 +334,7 @@ cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s) {
   const int rows_seq = a.q_len * a.groups;
   const int tiles_per_seq = (rows_seq + kPfRows - 1) / kPfRows;
   const int ranges = (a.max_blocks + kPfKb - 1) / kPfKb;
-  cudaError_t e = cudaFuncSetAttribute(prefill_indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kPfSmem));
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_indexer_kernel), kPfSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

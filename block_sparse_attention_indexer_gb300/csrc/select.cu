@@ -204,8 +204,7 @@ cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
   // are read from L2 on each pass
   a.row_cap = a.max_blocks < 4096 ? a.max_blocks : 4096;
   const size_t smem = static_cast<size_t>(kSelWarps) * a.row_cap * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(select_kernel), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((nrows + kSelWarps - 1) / kSelWarps));
