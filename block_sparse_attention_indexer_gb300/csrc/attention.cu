@@ -36,7 +36,8 @@ namespace msa {
 
 constexpr int kTeams = 3;                                 // teams per CTA
 constexpr int kTW = 4;                                    // warps per team (one 32-key quarter each)
-constexpr int kAW = kTeams * kTW;                         // warps per CTA
+constexpr int kAW = kTeams * kTW;                         // consuming warps per CTA
+constexpr int kAttnThreads = (kAW + kTeams) * 32;         // + one producer warp per team
 constexpr int kTSl = 3;                                   // page slots per team
 constexpr int kSlotBytes = 2 * (kPageData + kPageScale);  // K data | K scales | V data | V scales
 constexpr int kHeadsMax = 8;
@@ -52,59 +53,70 @@ struct TeamBars {
   uint64_t freed;        // every warp finished reading the merge area: kTW arrives
 };
 struct ItemMeta {
-  int64_t row;  // row of the item, -1 = end of the team's items
+  int row;      // row of the item, -1 = end of the team's items
   int blk;      // logical block (page items)
   int page;     // page id, -1 = no page (a row with nothing to attend to)
+  int pos;      // query position of the row (page items)
 };
 
+// Shared memory: page slots | mbarriers | per-warp merge areas | item metadata.  Every region
+// starts on a 16-byte boundary (the slots take bulk copies, the barriers need 8 bytes).
+constexpr size_t kSlotsBytes = static_cast<size_t>(kTeams) * kTSl * kSlotBytes;
+constexpr size_t kBarsBytes = (static_cast<size_t>(kTeams) * sizeof(TeamBars) + 15) / 16 * 16;
+constexpr size_t kRedBytes = static_cast<size_t>(kAW) * kRedFloats * sizeof(float);
+static_assert(kSlotsBytes % 16 == 0 && kRedBytes % 16 == 0, "attention shared-memory regions must stay 16-byte aligned");
+
 __host__ __device__ constexpr size_t attn_smem_bytes() {
-  return static_cast<size_t>(kTeams) * kTSl * kSlotBytes +
-         static_cast<size_t>(kAW) * kRedFloats * sizeof(float) +
-         static_cast<size_t>(kTeams) * kTSl * sizeof(ItemMeta) + static_cast<size_t>(kTeams) * sizeof(TeamBars);
+  return kSlotsBytes + kBarsBytes + kRedBytes + static_cast<size_t>(kTeams) * kTSl * sizeof(ItemMeta);
 }
 
-__host__ __device__ __forceinline__ int64_t range_lo(int64_t E, int c, int NC) { return E * c / NC; }
-__host__ __device__ __forceinline__ int owner_of(int64_t E, int64_t x, int NC) {
-  return static_cast<int>(((x + 1) * NC - 1) / E);
+// Team c of NC owns the entries [range_lo(c), range_lo(c + 1)) of the E = rows * 16 entries.
+__host__ __device__ __forceinline__ int range_lo(int E, int c, int NC) {
+  return static_cast<int>(static_cast<int64_t>(E) * c / NC);
+}
+__host__ __device__ __forceinline__ int owner_of(int E, int x, int NC) {
+  return static_cast<int>((static_cast<int64_t>(x + 1) * NC - 1) / E);
 }
 
+// Row bookkeeping in 32-bit arithmetic: rows = batch * q_len * groups < 2^20 (the host
+// bounds batch * q_len by 65535 and groups by 8), entries and head rows < 2^23.  The query
+// heads of row (b, t, g) are the head rows row * heads_per_group + h.
 struct RowInfo {
   int b, t, g, r, L;
   bool ok;
-  int64_t head_row0;
 };
 
-__device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int64_t row) {
+__device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int row) {
   RowInfo ri;
-  const int T = a.q_len, G = a.groups;
-  ri.b = static_cast<int>(row / (static_cast<int64_t>(T) * G));
-  ri.t = static_cast<int>((row / G) % T);
-  ri.g = static_cast<int>(row % G);
+  const unsigned T = static_cast<unsigned>(a.q_len), G = static_cast<unsigned>(a.groups);
+  const unsigned bt = static_cast<unsigned>(row) / G;
+  ri.g = static_cast<int>(static_cast<unsigned>(row) - bt * G);
+  ri.b = static_cast<int>(bt / T);
+  ri.t = static_cast<int>(bt - static_cast<unsigned>(ri.b) * T);
   ri.L = a.seq_lens[ri.b];
-  ri.ok = ri.L > 0 && ri.L >= T && ri.L <= static_cast<int64_t>(a.max_blocks) * kBlock;
-  ri.r = ri.ok ? (ri.L - T + ri.t) / kBlock : -1;
-  ri.head_row0 = (row / G) * (static_cast<int64_t>(G) * a.heads_per_group) + static_cast<int64_t>(ri.g) *
-                 a.heads_per_group;
+  ri.ok = ri.L > 0 && ri.L >= a.q_len && ri.L <= static_cast<int64_t>(a.max_blocks) * kBlock;
+  ri.r = ri.ok ? (ri.L - a.q_len + ri.t) / kBlock : -1;
   return ri;
 }
 
-// Resolves entries x = first + stride*(base + lane) (lane-parallel): page id (or -1 if the
-// entry is empty, past the recent block, or its block-table entry is bad) and block index.
-__device__ __forceinline__ void resolve_batch(const AttnArgs& a, int64_t first, int stride, int base, int count,
-                                              int lane, int& page, int& blk) {
+// Resolves entries x = first + base + lane (lane-parallel): page id (or -1 if the entry is
+// empty, past the recent block, or its block-table entry is bad) and block index.
+__device__ __forceinline__ void resolve_batch(const AttnArgs& a, int first, int base, int count, int lane, int& page,
+                                              int& blk, int& pos) {
   page = -1;
   blk = -1;
+  pos = -1;
   const int k = base + lane;
   if (k < count) {
-    const int64_t x = first + static_cast<int64_t>(stride) * k;
-    const int64_t row = x / kTopK;
-    const RowInfo ri = row_info(a, row);
+    const int x = first + k;
+    const RowInfo ri = row_info(a, x / kTopK);
     const int n = a.selection[x];
     if (ri.ok && n >= 0 && n <= ri.r) {
       const int p = a.block_table[static_cast<int64_t>(ri.b) * a.max_blocks + n];
       if (p >= 0 && p < a.num_pages) {
         page = p;
         blk = n;
+        pos = ri.L - a.q_len + ri.t;
       } else {
         flag_error(a.err, MSA_DEVERR_BAD_PAGE);
       }
@@ -112,10 +124,74 @@ __device__ __forceinline__ void resolve_batch(const AttnArgs& a, int64_t first, 
   }
 }
 
-__device__ __forceinline__ void load_q_raw(const AttnArgs& a, int64_t head_row0, bool ok, int gq, int t4, uint4& q0,
-                                           uint4& q1) {
-  if (ok && gq < a.heads_per_group) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.q + (head_row0 + gq) * kDim + 32 * t4);
+// Producer state of one team: its entry range, the scan position, the lane-held results of
+// the current batch of 32 resolved entries, and the number of items sent.
+struct TeamProd {
+  int x0, nk, pk, pb, produced;
+  int p_page, p_blk, p_pos;
+  bool seg_any, end_sent;
+};
+
+// Sends the team's next item into slot `produced % kTSl` (which the caller found free): the
+// next entry with a page (its K and V pages by bulk copy), a marker item for a row segment
+// with nothing to attend to, or, after the last entry, the end item.
+__device__ __forceinline__ void produce_one(const AttnArgs& a, TeamProd& st, uint8_t* slots, ItemMeta* meta,
+                                            TeamBars* tb, int lane) {
+  const int slot = st.produced % kTSl;
+  const int x1 = st.x0 + st.nk;
+  while (st.pk < st.nk) {
+    const int bi = st.pk >> 5;
+    if (bi != st.pb) {
+      resolve_batch(a, st.x0, bi * 32, st.nk, lane, st.p_page, st.p_blk, st.p_pos);
+      st.pb = bi;
+    }
+    const int page = __shfl_sync(0xffffffffu, st.p_page, st.pk & 31);
+    const int blk = __shfl_sync(0xffffffffu, st.p_blk, st.pk & 31);
+    const int pos = __shfl_sync(0xffffffffu, st.p_pos, st.pk & 31);
+    const int x = st.x0 + st.pk;
+    ++st.pk;
+    const bool last_in_seg = ((x + 1) % kTopK == 0) || (x + 1 == x1);
+    const bool emit = page >= 0 || (last_in_seg && !st.seg_any);
+    st.seg_any = last_in_seg ? false : (st.seg_any || page >= 0);
+    if (!emit) continue;
+    if (lane == 0) {
+      uint64_t* bar = &tb->full[slot];
+      meta[slot].row = x / kTopK;
+      meta[slot].blk = blk;
+      meta[slot].page = page;
+      meta[slot].pos = pos;
+      if (page >= 0) {
+        uint8_t* dst = slots + slot * kSlotBytes;
+        const int64_t pg = static_cast<int64_t>(page) * a.groups + (x / kTopK) % a.groups;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, kSlotBytes);
+        bulk_g2s(dst, a.k_data + pg * kPageData, kPageData, bar);
+        bulk_g2s(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar);
+        bulk_g2s(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar);
+        bulk_g2s(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar);
+      } else {
+        mbar_arrive(bar);
+      }
+    }
+    ++st.produced;
+    return;
+  }
+  if (lane == 0) {
+    meta[slot].row = -1;
+    meta[slot].blk = -1;
+    meta[slot].page = -1;
+    meta[slot].pos = -1;
+    mbar_arrive(&tb->full[slot]);
+  }
+  st.end_sent = true;
+  ++st.produced;
+}
+
+// The raw FP8 queries of head row gq of a group's row (lane: 32 bytes of dims 32 t4 ..).
+__device__ __forceinline__ void load_q_raw(const AttnArgs& a, int row, int gq, int t4, uint4& q0, uint4& q1) {
+  if (gq < a.heads_per_group) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.q + (static_cast<int64_t>(row) * a.heads_per_group + gq) * kDim + 32 * t4);
     q0 = __ldg(src);
     q1 = __ldg(src + 1);
   } else {
@@ -243,18 +319,17 @@ __device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n,
   }
 }
 
-__device__ __forceinline__ void write_out(const AttnArgs& a, int64_t head_row, int d, float num, float den,
-                                          float M) {
+__device__ __forceinline__ void write_out(const AttnArgs& a, int head_row, int d, float num, float den, float M) {
   const float v = den > 0.f ? num / den : 0.f;
-  a.out[head_row * kDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  a.out[static_cast<int64_t>(head_row) * kDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   if (d == 0 && a.lse != nullptr) a.lse[head_row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
-__global__ void __launch_bounds__(kAW * 32, 1) attention_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(kTeams) * kTSl * kSlotBytes);
-  ItemMeta* meta = reinterpret_cast<ItemMeta*>(red + kAW * kRedFloats);
-  TeamBars* tbars = reinterpret_cast<TeamBars*>(meta + kTeams * kTSl);
+  TeamBars* tbars = reinterpret_cast<TeamBars*>(smem + kSlotsBytes);
+  float* red = reinterpret_cast<float*>(smem + kSlotsBytes + kBarsBytes);
+  ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + kSlotsBytes + kBarsBytes + kRedBytes);
 
   // launched as a programmatic dependent of the previous kernel on the stream (the
   // selection): wait for it and its memory before touching global memory
@@ -262,98 +337,71 @@ __global__ void __launch_bounds__(kAW * 32, 1) attention_kernel(const AttnArgs a
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, t4 = lane & 3;
-  const int team = warp / kTW, wt = warp % kTW;
   const int Hg = a.heads_per_group;
-  const int NT = gridDim.x * kTeams, tt = blockIdx.x * kTeams + team;
-  const int64_t rows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
-  const int64_t E = rows * kTopK;
-  const int64_t x0 = range_lo(E, tt, NT), x1 = range_lo(E, tt + 1, NT);
-  const int64_t R0 = x0 / kTopK;
-
-  uint8_t* my_slots = smem + static_cast<size_t>(team) * kTSl * kSlotBytes;
-  ItemMeta* my_meta = meta + team * kTSl;
-  TeamBars* tb = tbars + team;
-  float* team_red = red + team * kTW * kRedFloats;
-  if (wt == 0 && lane == 0) {
+  const int NT = gridDim.x * kTeams;
+  const int rows = a.batch * a.q_len * a.groups;
+  const int E = rows * kTopK;
+  if (tid < kTeams) {
+    TeamBars* tb = tbars + tid;
     for (int i = 0; i < kTSl; ++i) {
       mbar_init(&tb->full[i], 1);
       mbar_init(&tb->empty[i], kTW);
     }
     mbar_init(&tb->merged, kTW);
     mbar_init(&tb->freed, kTW);
-    fence_mbar_init();
   }
+  fence_mbar_init();
   __syncthreads();
 
-  // ---- producer (warp 0 of the team): entries of [x0, x1) in order; an item per page to
-  // attend to, one marker item for a row segment with none, and a final end item
-  const int64_t nk = x1 - x0;
-  int64_t pk = 0;
-  int pb = -1, p_page = -1, p_blk = -1;
-  bool seg_any = false, end_sent = false;
-  int produced = 0;
-  auto produce_one = [&]() {
-    const int slot = produced % kTSl;
-    while (pk < nk) {
-      const int bi = static_cast<int>(pk >> 5);
-      if (bi != pb) {
-        resolve_batch(a, x0, 1, bi * 32, static_cast<int>(nk), lane, p_page, p_blk);
-        pb = bi;
+  if (warp >= kAW) {
+    // ---- producer of team `tm`: its items in order, each into the next slot once the
+    // team's four warps have released it
+    const int tm = warp - kAW;
+    const int tt = blockIdx.x * kTeams + tm;
+    TeamBars* tb = tbars + tm;
+    TeamProd st;
+    st.x0 = range_lo(E, tt, NT);
+    st.nk = range_lo(E, tt + 1, NT) - st.x0;
+    st.pk = 0;
+    st.pb = -1;
+    st.produced = 0;
+    st.seg_any = false;
+    st.end_sent = false;
+    bool failed = false;
+    while (!st.end_sent) {
+      const int slot = st.produced % kTSl;
+      if (st.produced >= kTSl && !mbar_wait_warp(&tb->empty[slot], ((st.produced / kTSl) - 1) & 1)) {
+        failed = true;
+        break;
       }
-      const int page = __shfl_sync(0xffffffffu, p_page, static_cast<int>(pk & 31));
-      const int blk = __shfl_sync(0xffffffffu, p_blk, static_cast<int>(pk & 31));
-      const int64_t x = x0 + pk;
-      ++pk;
-      const bool last_in_seg = ((x + 1) % kTopK == 0) || (x + 1 == x1);
-      const bool emit = page >= 0 || (last_in_seg && !seg_any);
-      seg_any = last_in_seg ? false : (seg_any || page >= 0);
-      if (!emit) continue;
-      if (lane == 0) {
-        uint64_t* bar = &tb->full[slot];
-        my_meta[slot].row = x / kTopK;
-        my_meta[slot].blk = blk;
-        my_meta[slot].page = page;
-        if (page >= 0) {
-          uint8_t* dst = my_slots + slot * kSlotBytes;
-          const int64_t pg = static_cast<int64_t>(page) * a.groups + (x / kTopK) % a.groups;
-          fence_proxy_async_smem();
-          mbar_arrive_expect_tx(bar, kSlotBytes);
-          bulk_g2s(dst, a.k_data + pg * kPageData, kPageData, bar);
-          bulk_g2s(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar);
-          bulk_g2s(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar);
-          bulk_g2s(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar);
-        } else {
-          mbar_arrive(bar);
-        }
-      }
-      ++produced;
-      return;
+      produce_one(a, st, smem + static_cast<size_t>(tm) * kTSl * kSlotBytes, meta + tm * kTSl, tb, lane);
     }
-    if (!end_sent) {
-      if (lane == 0) {
-        my_meta[slot].row = -1;
-        my_meta[slot].blk = -1;
-        my_meta[slot].page = -1;
-        mbar_arrive(&tb->full[slot]);
-      }
-      end_sent = true;
-      ++produced;
+    if (failed) {
+      if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
+      // wait (bounded) for the copies still in flight before leaving
+      for (int k = max(0, st.produced - kTSl); k < st.produced; ++k) mbar_wait(&tb->full[k % kTSl], (k / kTSl) & 1);
     }
-  };
-  if (wt == 0)
-    for (int s = 0; s < kTSl && !end_sent; ++s) produce_one();
+    return;
+  }
 
-  // ---- consumers (all four warps)
+  // ---- consumers: team `team`, warp wt of it (one 32-key quarter of every page)
+  const int team = warp / kTW, wt = warp % kTW;
+  const int tt = blockIdx.x * kTeams + team;
+  const int x0 = range_lo(E, tt, NT), x1 = range_lo(E, tt + 1, NT);
+  const int R0 = x0 / kTopK;
+  uint8_t* my_slots = smem + static_cast<size_t>(team) * kTSl * kSlotBytes;
+  ItemMeta* my_meta = meta + team * kTSl;
+  TeamBars* tb = tbars + team;
+  float* team_red = red + team * kTW * kRedFloats;
+
   int consumed = 0, nseg = 0;
-  int64_t cur_row = -2;
-  RowInfo ri = {};
-  int pos = 0;
+  int cur_row = -2;
   uint32_t bq[8][2] = {};
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float o[8][4] = {};
   bool failed = false;
 
-  auto finalize = [&](int64_t R) -> bool {
+  auto finalize = [&](int R) -> bool {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       float v = l_run[e];
@@ -381,30 +429,30 @@ __global__ void __launch_bounds__(kAW * 32, 1) attention_kernel(const AttnArgs a
     if (!mbar_wait_warp(&tb->merged, nseg & 1)) return false;
     const bool whole = R * kTopK >= x0 && (R + 1) * kTopK <= x1;
     float* slot_part = whole ? nullptr : a.partial + static_cast<int64_t>(2 * tt + (R == R0 ? 0 : 1)) * kSlotFloats;
+    // lane (w, h) = (lane >> 3, lane & 7): weight e^{m_w - M} of warp w's state for head h,
+    // with M the heads' maximum over the team's warps, and the weighted sum of the l's
+    const float* stats = team_red + kHeadsMax * kDim;
+    const int lw = lane >> 3, lh = lane & 7;
+    const float mw = stats[lw * kRedFloats + lh];
+    float Mh = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 8));
+    Mh = fmaxf(Mh, __shfl_xor_sync(0xffffffffu, Mh, 16));
+    const float fw = (mw == -INFINITY) ? 0.f : exp2f(mw - Mh);
+    float den = fw * stats[lw * kRedFloats + kHeadsMax + lh];
+    den += __shfl_xor_sync(0xffffffffu, den, 8);
+    den += __shfl_xor_sync(0xffffffffu, den, 16);
     const int d = wt * 32 + lane;  // each warp merges 32 of the 128 dims
     for (int h = 0; h < Hg; ++h) {
-      float M = -INFINITY;
+      float num = 0.f;
 #pragma unroll
-      for (int w = 0; w < kTW; ++w) M = fmaxf(M, team_red[w * kRedFloats + kHeadsMax * kDim + h]);
-      float num = 0.f, den = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kTW; ++w) {
-          const float mw = team_red[w * kRedFloats + kHeadsMax * kDim + h];
-          if (mw != -INFINITY) {
-            const float f = exp2f(mw - M);
-            num += f * team_red[w * kRedFloats + h * kDim + d];
-            den += f * team_red[w * kRedFloats + kHeadsMax * kDim + kHeadsMax + h];
-          }
-        }
-      }
+      for (int w = 0; w < kTW; ++w) num += __shfl_sync(0xffffffffu, fw, w * 8 + h) * team_red[w * kRedFloats + h * kDim + d];
+      const float M = __shfl_sync(0xffffffffu, Mh, h), dh = __shfl_sync(0xffffffffu, den, h);
       if (whole) {
-        write_out(a, ri.head_row0 + h, d, num, den, M);
+        write_out(a, R * Hg + h, d, num, dh, M);
       } else {
         slot_part[h * (kDim + 2) + d] = num;
         if (d == 0) {
           slot_part[h * (kDim + 2) + kDim] = M;
-          slot_part[h * (kDim + 2) + kDim + 1] = den;
+          slot_part[h * (kDim + 2) + kDim + 1] = dh;
         }
       }
     }
@@ -414,31 +462,34 @@ __global__ void __launch_bounds__(kAW * 32, 1) attention_kernel(const AttnArgs a
     return true;
   };
 
-  uint4 qn0 = make_uint4(0u, 0u, 0u, 0u), qn1 = qn0;  // next row's raw FP8 queries
-  int64_t q_row = -1;
+  // the first row's queries load while the first pages are on their way; later rows'
+  // are prefetched one row ahead (the rows of a range are consecutive)
+  uint4 qn0 = make_uint4(0u, 0u, 0u, 0u), qn1 = qn0;
+  int q_row = -1;
+  if (x0 < x1) {
+    load_q_raw(a, R0, gq, t4, qn0, qn1);
+    q_row = R0;
+  }
   while (true) {
     const int slot = consumed % kTSl;
     if (!mbar_wait_warp(&tb->full[slot], (consumed / kTSl) & 1)) {
       failed = true;
       break;
     }
-    const int64_t row = my_meta[slot].row;
+    const int row = my_meta[slot].row;
     const int blk = my_meta[slot].blk;
     const int page = my_meta[slot].page;
+    const int pos = my_meta[slot].pos;
     if (row != cur_row) {
       if (cur_row >= 0 && !finalize(cur_row)) {
         failed = true;
         break;
       }
       if (row >= 0) {
-        ri = row_info(a, row);
-        pos = ri.L - a.q_len + ri.t;
-        if (q_row != row) load_q_raw(a, ri.head_row0, ri.ok, gq, t4, qn0, qn1);
+        if (q_row != row) load_q_raw(a, row, gq, t4, qn0, qn1);
         q_fragments(qn0, qn1, bq);
-        // prefetch the next row's queries (rows of a range are consecutive)
         if ((row + 1) * kTopK < x1) {
-          const RowInfo rn = row_info(a, row + 1);
-          load_q_raw(a, rn.head_row0, rn.ok, gq, t4, qn0, qn1);
+          load_q_raw(a, row + 1, gq, t4, qn0, qn1);
           q_row = row + 1;
         }
         m_run[0] = m_run[1] = -INFINITY;
@@ -449,48 +500,62 @@ __global__ void __launch_bounds__(kAW * 32, 1) attention_kernel(const AttnArgs a
       cur_row = row;
     }
     if (page >= 0)
-      attend_quarter(my_slots + slot * kSlotBytes, wt, blk, ri.r, pos, a.scale_log2, gq, t4, bq, m_run, l_run, o);
+      attend_quarter(my_slots + slot * kSlotBytes, wt, blk, pos / kBlock, pos, a.scale_log2, gq, t4, bq, m_run, l_run,
+                     o);
     __syncwarp();
     if (lane == 0) mbar_arrive(&tb->empty[slot]);
     ++consumed;
     if (row < 0) break;
-    if (wt == 0 && !end_sent) {  // refill the slot just consumed once every warp is done with it
-      if (!mbar_wait_warp(&tb->empty[slot], ((consumed - 1) / kTSl) & 1)) {
-        failed = true;
-        break;
-      }
-      produce_one();
-    }
   }
-
   if (failed && lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
-  // the producer drains its copies still in flight (only after a timeout; bounded)
-  if (wt == 0)
-    for (int k = consumed; k < produced; ++k) mbar_wait(&tb->full[k % kTSl], (k / kTSl) & 1);
 }
 
 // Rows cut by team-range boundaries: combine the partial states the teams left.  One CTA per
-// boundary (the first boundary inside a row owns the row), one thread per (head, dim), one
-// online pass over the row's segments so that all their loads are in flight together.
+// boundary (the first boundary inside a row owns the row); its first warp lists the row's
+// partial slots in shared memory, then one thread per (head, dim) makes one online pass over
+// them, so that all their loads are in flight together.
 __global__ void __launch_bounds__(kHeadsMax * kDim) merge_kernel(const AttnArgs a, int NT) {
+  __shared__ int s_slot[kTopK];
+  __shared__ int s_n, s_row;
   grid_dependency_wait();
-  const int k = blockIdx.x + 1;  // boundary between ranges k-1 and k
-  const int64_t rows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
-  const int64_t E = rows * kTopK;
-  const int64_t xb = range_lo(E, k, NT);
-  if (xb % kTopK == 0 || xb >= E) return;  // not inside a row
-  const int64_t R = xb / kTopK;
-  if (range_lo(E, k - 1, NT) > R * kTopK) return;  // an earlier boundary inside this row owns it
-  const int ca = owner_of(E, R * kTopK, NT), cbk = owner_of(E, R * kTopK + kTopK - 1, NT);
-  const int h = threadIdx.x / kDim, d = threadIdx.x % kDim;
-  if (h >= a.heads_per_group) return;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 32) {
+    const int k = blockIdx.x + 1;  // boundary between ranges k-1 and k
+    const int E = a.batch * a.q_len * a.groups * kTopK;
+    const int xb = range_lo(E, k, NT);
+    int R = -1, ca = 0, cb = -1;
+    // inside a row, and no earlier boundary inside the same row
+    if (xb % kTopK != 0 && xb < E && range_lo(E, k - 1, NT) <= (xb / kTopK) * kTopK) {
+      R = xb / kTopK;
+      ca = owner_of(E, R * kTopK, NT);
+      cb = owner_of(E, R * kTopK + kTopK - 1, NT);
+    }
+    int n = 0;
+    for (int c0 = ca; c0 <= cb; c0 += 32) {  // the non-empty ranges among ca..cb, in order
+      const int c = c0 + lane;
+      int slot = -1;
+      if (c <= cb) {
+        const int lo = range_lo(E, c, NT), hi = range_lo(E, c + 1, NT);
+        if (lo < hi) slot = 2 * c + ((lo / kTopK) == R ? 0 : 1);
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, slot >= 0);
+      const int idx = n + __popc(m & ((1u << lane) - 1u));
+      if (slot >= 0 && idx < kTopK) s_slot[idx] = slot;
+      n += __popc(m);
+    }
+    if (lane == 0) {
+      s_n = min(n, kTopK);
+      s_row = R;
+    }
+  }
+  __syncthreads();
+  const int R = s_row, n = s_n;
+  const int h = tid / kDim, d = tid % kDim;
+  if (R < 0 || h >= a.heads_per_group) return;
   float M = -INFINITY, num = 0.f, den = 0.f;
 #pragma unroll 4
-  for (int cc = ca; cc <= cbk; ++cc) {
-    const int64_t lo = range_lo(E, cc, NT), hi = range_lo(E, cc + 1, NT);
-    if (lo >= hi) continue;  // empty range
-    const float* part =
-        a.partial + static_cast<int64_t>(2 * cc + ((lo / kTopK) == R ? 0 : 1)) * kSlotFloats + h * (kDim + 2);
+  for (int i = 0; i < n; ++i) {
+    const float* part = a.partial + static_cast<int64_t>(s_slot[i]) * kSlotFloats + h * (kDim + 2);
     const float ms = __ldcg(part + kDim), ls = __ldcg(part + kDim + 1), os = __ldcg(part + d);
     if (ms == -INFINITY) continue;
     if (ms > M) {
@@ -504,8 +569,7 @@ __global__ void __launch_bounds__(kHeadsMax * kDim) merge_kernel(const AttnArgs 
       den += f * ls;
     }
   }
-  const RowInfo ri = row_info(a, R);
-  write_out(a, ri.head_row0 + h, d, num, den, M);
+  write_out(a, R * a.heads_per_group + h, d, num, den, M);
 }
 
 size_t attn_partial_bytes() {
@@ -524,7 +588,7 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(NC);
-  cfg.blockDim = dim3(kAW * 32);
+  cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;

@@ -44,8 +44,9 @@ struct PfShared {
   int32_t pages[kPfKb];
 };
 
+constexpr int kSbufLd = kPfKb + 1;        // score buffer row stride (odd: conflict-free column writes)
 constexpr size_t kPfSmem = 1024 /* alignment slack */ + 2 * kHalfTile /* Q */ + kPfKSt * 2 * kHalfTile /* K */ +
-                           kPfRawSt * kRawBytes + kPfRows * kPfKb * sizeof(float) + sizeof(PfShared);
+                           kPfRawSt * kRawBytes + kPfRows * kSbufLd * sizeof(float) + sizeof(PfShared);
 
 // byte offset of 16-byte chunk `chunk` (0..7) of row r in a K-major SW128 tile of 128-byte rows
 __device__ __forceinline__ uint32_t sw128(int r, int chunk) {
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
   uint8_t* k_tiles = q_tile + 2 * kHalfTile;                // [stage] B0 | B1
   uint8_t* raw = k_tiles + kPfKSt * 2 * kHalfTile;          // [stage] 9 KB
   float* sbuf = reinterpret_cast<float*>(raw + kPfRawSt * kRawBytes);  // [128][kPfKb]
-  PfShared* sh = reinterpret_cast<PfShared*>(sbuf + kPfRows * kPfKb);
+  PfShared* sh = reinterpret_cast<PfShared*>(sbuf + kPfRows * kSbufLd);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.q_len, G = a.groups;
@@ -221,8 +222,15 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
         }
         const uint8_t* src = raw + s * kRawBytes;
         uint8_t* kdst = k_tiles + ks * 2 * kHalfTile;
+        // items (row, 32-dim chunk c) in octets (8 lanes = one shared-memory phase of 16-byte
+        // accesses): two octets share a group of 4 rows, lane i of octet o takes chunk
+        // c = i >> 1 of row 4 (o >> 1) + (i & 1) + 2 (((i >> 1) & 1) ^ (o & 1)).  An octet's
+        // loads then hit 8 distinct 16-byte bank groups (row parity x chunk), and with the chunk
+        // order of the upper half of the dims rotated by 2 so do its swizzled stores
         for (int item = dt; item < kPfRows * 4; item += 128) {
-          const int r = item >> 2, c = item & 3;  // 16 packed bytes = dims 32c .. 32c+31
+          const int i8 = item & 7, oct = item >> 3;
+          const int r = 4 * (oct >> 1) + (i8 & 1) + 2 * (((i8 >> 1) & 1) ^ (oct & 1));
+          const int c = i8 >> 1;  // dims 32c .. 32c+31
           const uint4 d = lds128(src + r * kRowBytes + 16 * c);
           const uint32_t sc = lds16(src + kPageData + r * kRowScales + 2 * c);
           const uint32_t s0 = e4m3_bcast_f16x2(sc, 0), s1 = e4m3_bcast_f16x2(sc, 1);
@@ -237,10 +245,14 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
           }
           uint8_t* tdst = kdst + (c < 2 ? 0 : kHalfTile);
           const int ch = 4 * (c & 1);
+          const bool rot = c >= 2;  // store q writes chunk q ^ 2 in the upper half
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(tdst + sw128(r, ch + q)) =
-                make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) {
+            const int qq = q ^ 2;
+            const uint4 v = rot ? make_uint4(h[4 * qq], h[4 * qq + 1], h[4 * qq + 2], h[4 * qq + 3])
+                                : make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+            *reinterpret_cast<uint4*>(tdst + sw128(r, ch + (rot ? qq : q))) = v;
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
-        sbuf[r * kPfKb + k] = (row_ok && sh->pages[k] >= 0) ? mx : -INFINITY;
+        sbuf[r * kSbufLd + k] = (row_ok && sh->pages[k] >= 0) ? mx : -INFINITY;
       }
     }
   }
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
       const int r = warp * 32 + i;
       const int n = n0 + lane;
       if (r < nrows && n < a.max_blocks)
-        a.block_scores[(grow0 + r) * a.max_blocks + n] = lane < nblk ? sbuf[r * kPfKb + lane] : -INFINITY;
+        a.block_scores[(grow0 + r) * a.max_blocks + n] = lane < nblk ? sbuf[r * kSbufLd + lane] : -INFINITY;
     }
   }
   if (failed && lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
