@@ -281,7 +281,9 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
   float* partial = reinterpret_cast<float*>(ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch));
   cudaError_t e = run_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
   if (e == cudaSuccess) e = launch_select(select_args(cfg, batch, scores, sel), s);
-  if (e == cudaSuccess) e = launch_attention(attn_args(cfg, cache, batch, q, sel, out, lse, partial, err), sms, s);
+  AttnArgs aa = attn_args(cfg, cache, batch, q, sel, out, lse, partial, err);
+  aa.q_early = 1;  // the kernel before it is this step's selection
+  if (e == cudaSuccess) e = launch_attention(aa, sms, s);
   return cuda_status(e);
 }
 

@@ -331,10 +331,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
   float* red = reinterpret_cast<float*>(smem + kSlotsBytes + kBarsBytes);
   ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + kSlotsBytes + kBarsBytes + kRedBytes);
 
-  // launched as a programmatic dependent of the previous kernel on the stream (the
-  // selection): wait for it and its memory before touching global memory
-  grid_dependency_wait();
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, t4 = lane & 3;
   const int Hg = a.heads_per_group;
@@ -353,7 +349,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
   fence_mbar_init();
   __syncthreads();
 
+  // Launched as a programmatic dependent of the previous kernel on the stream (the
+  // selection): the prologue above, and on the fused decode path the consumers' first
+  // queries below, run before that kernel has finished; everything that reads what it
+  // writes comes after this wait.
   if (warp >= kAW) {
+    grid_dependency_wait();
+    grid_dependents_launch();  // the merge kernel may be scheduled as SMs free up
     // ---- producer of team `tm`: its items in order, each into the next slot once the
     // team's four warps have released it
     const int tm = warp - kAW;
@@ -464,12 +466,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
 
   // the first row's queries load while the first pages are on their way; later rows'
   // are prefetched one row ahead (the rows of a range are consecutive)
+  // (early only when the kernel before this one is the selection of the same decode step:
+  // the queries were then written before that step's first kernel, which waited for them)
   uint4 qn0 = make_uint4(0u, 0u, 0u, 0u), qn1 = qn0;
   int q_row = -1;
+  if (!a.q_early) grid_dependency_wait();
   if (x0 < x1) {
     load_q_raw(a, R0, gq, t4, qn0, qn1);
     q_row = R0;
   }
+  if (a.q_early) grid_dependency_wait();
+  grid_dependents_launch();
   while (true) {
     const int slot = consumed % kTSl;
     if (!mbar_wait_warp(&tb->full[slot], (consumed / kTSl) & 1)) {
@@ -512,12 +519,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
 
 // Rows cut by team-range boundaries: combine the partial states the teams left.  One CTA per
 // boundary (the first boundary inside a row owns the row); its first warp lists the row's
-// partial slots in shared memory, then one thread per (head, dim) makes one online pass over
+// partial slots in shared memory (arithmetic only, so it runs before the wait on the
+// attention kernel), then one thread per (head, pair of dims) makes one online pass over
 // them, so that all their loads are in flight together.
-__global__ void __launch_bounds__(kHeadsMax * kDim) merge_kernel(const AttnArgs a, int NT) {
+constexpr int kMergeThreads = kHeadsMax * kDim / 2;
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a, int NT) {
   __shared__ int s_slot[kTopK];
   __shared__ int s_n, s_row;
-  grid_dependency_wait();
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
     const int k = blockIdx.x + 1;  // boundary between ranges k-1 and k
@@ -550,26 +559,32 @@ __global__ void __launch_bounds__(kHeadsMax * kDim) merge_kernel(const AttnArgs 
   }
   __syncthreads();
   const int R = s_row, n = s_n;
-  const int h = tid / kDim, d = tid % kDim;
+  const int h = tid / (kDim / 2), d = 2 * (tid % (kDim / 2));
   if (R < 0 || h >= a.heads_per_group) return;
-  float M = -INFINITY, num = 0.f, den = 0.f;
+  grid_dependency_wait();  // the attention kernel's partial states
+  float M = -INFINITY, num0 = 0.f, num1 = 0.f, den = 0.f;
 #pragma unroll 4
   for (int i = 0; i < n; ++i) {
     const float* part = a.partial + static_cast<int64_t>(s_slot[i]) * kSlotFloats + h * (kDim + 2);
-    const float ms = __ldcg(part + kDim), ls = __ldcg(part + kDim + 1), os = __ldcg(part + d);
+    const float ms = __ldcg(part + kDim), ls = __ldcg(part + kDim + 1);
+    const float2 os = __ldcg(reinterpret_cast<const float2*>(part + d));
     if (ms == -INFINITY) continue;
     if (ms > M) {
       const float f = (M == -INFINITY) ? 0.f : exp2f(M - ms);
-      num = num * f + os;
+      num0 = num0 * f + os.x;
+      num1 = num1 * f + os.y;
       den = den * f + ls;
       M = ms;
     } else {
       const float f = exp2f(ms - M);
-      num += f * os;
+      num0 += f * os.x;
+      num1 += f * os.y;
       den += f * ls;
     }
   }
-  write_out(a, R * a.heads_per_group + h, d, num, den, M);
+  const int head_row = R * a.heads_per_group + h;
+  write_out(a, head_row, d, num0, den, M);
+  write_out(a, head_row, d + 1, num1, den, M);
 }
 
 size_t attn_partial_bytes() {
@@ -598,7 +613,7 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s) {
   const int NT = NC * kTeams;
   cudaLaunchConfig_t mcfg = {};
   mcfg.gridDim = dim3(NT - 1);
-  mcfg.blockDim = dim3(kDim * a.heads_per_group);
+  mcfg.blockDim = dim3(kMergeThreads);
   mcfg.stream = s;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;

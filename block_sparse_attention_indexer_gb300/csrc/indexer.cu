@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
   // launched as a programmatic dependent of the previous kernel on the stream: wait for it
   // (and its memory) before touching global memory
   grid_dependency_wait();
+  grid_dependents_launch();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -386,6 +387,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
   __shared__ int32_t warp_tot[kHWarps];
 
   grid_dependency_wait();
+  grid_dependents_launch();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int T = a.q_len, G = a.groups;

@@ -98,6 +98,15 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // memory is visible (a no-op when there is no such kernel).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Lets the next kernel on the stream (launched with programmatic stream serialization) be
+// scheduled once every CTA of this grid has called it or exited; that kernel still reads
+// nothing of this one's before its grid_dependency_wait, which waits for this grid's
+// completion.  Called after this kernel's own grid_dependency_wait, so that everything
+// before this kernel on the stream has completed by the time the next one starts.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier + bulk copy
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -43,6 +43,7 @@ struct AttnArgs {
   float* lse;                  // [B][T][H] or null
   float* partial;              // attn_partial_bytes(): two partial-state slots per CTA
   float scale_log2;            // softmax_scale * log2(e)
+  int32_t q_early;             // 1: read the first queries before waiting on the previous kernel
   uint32_t* err;
 };
 

@@ -97,6 +97,7 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const IndexerArgs a, int tiles_per_seq) {
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
+  grid_dependents_launch();
 
   // carve shared memory (tiles 1024-byte aligned for the swizzle)
   const uint32_t base_u32 = smem_u32(smem_raw);

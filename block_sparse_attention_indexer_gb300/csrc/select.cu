@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs
   // launched as a programmatic dependent of the previous kernel on the stream: wait for it
   // (and its memory) before touching global memory
   grid_dependency_wait();
+  grid_dependents_launch();
   const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
   if (row >= nrows) return;
