@@ -45,6 +45,14 @@ constexpr int kRedFloats = kHeadsMax * kDim + 2 * kHeadsMax;   // one warp's o[8
 constexpr int kSlotFloats = kHeadsMax * (kDim + 2);             // one partial slot: [8][o 128, m, l]
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// 2^x by the hardware approximation (ex2.approx, relative error about 2^-22), subnormal
+// results flushed to zero: softmax weights below 2^-126 of the row maximum count as 0.
+__device__ __forceinline__ float exp2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // per team: slots, merge area, item metadata, barriers
 struct TeamBars {
   uint64_t full[kTSl];   // a page (or a marker item) is in the slot: 1 arrive (+ copy bytes)
@@ -99,92 +107,50 @@ __device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int row) {
   return ri;
 }
 
-// Resolves entries x = first + base + lane (lane-parallel): page id (or -1 if the entry is
-// empty, past the recent block, or its block-table entry is bad) and block index.
-__device__ __forceinline__ void resolve_batch(const AttnArgs& a, int first, int base, int count, int lane, int& page,
-                                              int& blk, int& pos) {
-  page = -1;
-  blk = -1;
-  pos = -1;
-  const int k = base + lane;
-  if (k < count) {
-    const int x = first + k;
-    const RowInfo ri = row_info(a, x / kTopK);
-    const int n = a.selection[x];
-    if (ri.ok && n >= 0 && n <= ri.r) {
-      const int p = a.block_table[static_cast<int64_t>(ri.b) * a.max_blocks + n];
-      if (p >= 0 && p < a.num_pages) {
-        page = p;
-        blk = n;
-        pos = ri.L - a.q_len + ri.t;
-      } else {
-        flag_error(a.err, MSA_DEVERR_BAD_PAGE);
-      }
+// Sends one item into the team's next slot once its four warps have released it: a page
+// (its K and V pages of KV head `row % groups`, by bulk copy), a marker (page -1: a row
+// segment with nothing to attend to) or the end (row -1).  False if the wait gave up.
+__device__ __forceinline__ bool send_item(const AttnArgs& a, int& produced, uint8_t* slots, ItemMeta* meta,
+                                          TeamBars* tb, int lane, int row, int blk, int page, int pos) {
+  const int slot = produced % kTSl;
+  if (produced >= kTSl && !mbar_wait_warp(&tb->empty[slot], ((produced / kTSl) - 1) & 1)) return false;
+  if (lane == 0) {
+    uint64_t* bar = &tb->full[slot];
+    meta[slot].row = row;
+    meta[slot].blk = blk;
+    meta[slot].page = page;
+    meta[slot].pos = pos;
+    if (page >= 0) {
+      uint8_t* dst = slots + slot * kSlotBytes;
+      const int64_t pg = static_cast<int64_t>(page) * a.groups + row % a.groups;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, kSlotBytes);
+      bulk_g2s(dst, a.k_data + pg * kPageData, kPageData, bar);
+      bulk_g2s(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar);
+      bulk_g2s(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar);
+      bulk_g2s(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar);
+    } else {
+      mbar_arrive(bar);
     }
   }
+  ++produced;
+  return true;
 }
 
-// Producer state of one team: its entry range, the scan position, the lane-held results of
-// the current batch of 32 resolved entries, and the number of items sent.
-struct TeamProd {
-  int x0, nk, pk, pb, produced;
-  int p_page, p_blk, p_pos;
-  bool seg_any, end_sent;
-};
-
-// Sends the team's next item into slot `produced % kTSl` (which the caller found free): the
-// next entry with a page (its K and V pages by bulk copy), a marker item for a row segment
-// with nothing to attend to, or, after the last entry, the end item.
-__device__ __forceinline__ void produce_one(const AttnArgs& a, TeamProd& st, uint8_t* slots, ItemMeta* meta,
-                                            TeamBars* tb, int lane) {
-  const int slot = st.produced % kTSl;
-  const int x1 = st.x0 + st.nk;
-  while (st.pk < st.nk) {
-    const int bi = st.pk >> 5;
-    if (bi != st.pb) {
-      resolve_batch(a, st.x0, bi * 32, st.nk, lane, st.p_page, st.p_blk, st.p_pos);
-      st.pb = bi;
-    }
-    const int page = __shfl_sync(0xffffffffu, st.p_page, st.pk & 31);
-    const int blk = __shfl_sync(0xffffffffu, st.p_blk, st.pk & 31);
-    const int pos = __shfl_sync(0xffffffffu, st.p_pos, st.pk & 31);
-    const int x = st.x0 + st.pk;
-    ++st.pk;
-    const bool last_in_seg = ((x + 1) % kTopK == 0) || (x + 1 == x1);
-    const bool emit = page >= 0 || (last_in_seg && !st.seg_any);
-    st.seg_any = last_in_seg ? false : (st.seg_any || page >= 0);
-    if (!emit) continue;
-    if (lane == 0) {
-      uint64_t* bar = &tb->full[slot];
-      meta[slot].row = x / kTopK;
-      meta[slot].blk = blk;
-      meta[slot].page = page;
-      meta[slot].pos = pos;
-      if (page >= 0) {
-        uint8_t* dst = slots + slot * kSlotBytes;
-        const int64_t pg = static_cast<int64_t>(page) * a.groups + (x / kTopK) % a.groups;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, kSlotBytes);
-        bulk_g2s(dst, a.k_data + pg * kPageData, kPageData, bar);
-        bulk_g2s(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar);
-        bulk_g2s(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar);
-        bulk_g2s(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar);
-      } else {
-        mbar_arrive(bar);
-      }
-    }
-    ++st.produced;
-    return;
+// The producer's view of one row: its selection (lane j < 16: block id of entry j) and the
+// page of each entry (-1: empty, past the recent block, or a bad block-table entry).
+__device__ __forceinline__ void row_pages(const AttnArgs& a, int R, int lane, int& blk, int& page, int& pos) {
+  const RowInfo ri = row_info(a, R);
+  blk = (ri.ok && lane < kTopK) ? a.selection[static_cast<int64_t>(R) * kTopK + lane] : -1;
+  page = -1;
+  pos = ri.L - a.q_len + ri.t;
+  if (lane < kTopK && ri.ok && blk >= 0 && blk <= ri.r) {
+    const int p = a.block_table[static_cast<int64_t>(ri.b) * a.max_blocks + blk];
+    if (p >= 0 && p < a.num_pages)
+      page = p;
+    else
+      flag_error(a.err, MSA_DEVERR_BAD_PAGE);
   }
-  if (lane == 0) {
-    meta[slot].row = -1;
-    meta[slot].blk = -1;
-    meta[slot].page = -1;
-    meta[slot].pos = -1;
-    mbar_arrive(&tb->full[slot]);
-  }
-  st.end_sent = true;
-  ++st.produced;
 }
 
 // The raw FP8 queries of head row gq of a group's row (lane: 32 bytes of dims 32 t4 ..).
@@ -216,20 +182,23 @@ __device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n,
   const uint8_t* vd = ks + kPageScale;
   const uint8_t* vs = vd + kPageData;
   const bool recent = (n == r);
-  // ---- S^T = K Q^T for 32 keys (two 16-key tiles)
+  // ---- S^T = K Q^T for 32 keys (two 16-key tiles), raw (unscaled) logits
   float x[2][4];
 #pragma unroll
   for (int mq = 0; mq < 2; ++mq) {
-    const int r0 = qk * 32 + mq * 16 + gq, r1 = r0 + 8;
+    // tile row i holds key pi(i) = (i & 8) | (i & 1) << 2 | (i >> 1) & 3 of the 16: the PV
+    // step's lanes then read V rows 1 apart (2-way bank conflicts instead of 4-way)
+    const int r0 = qk * 32 + mq * 16 + (((gq & 1) << 2) | (gq >> 1)), r1 = r0 + 8;
     const uint4 d0 = lds128(kd + r0 * kRowBytes + 16 * t4);
     const uint4 d1 = lds128(kd + r1 * kRowBytes + 16 * t4);
-    const uint32_t s0 = lds16(ks + r0 * kRowScales + 2 * t4);
-    const uint32_t s1 = lds16(ks + r1 * kRowScales + 2 * t4);
-    const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
-    const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
+    // the lane's two block scales of each row, as f16 pairs (s, s)
+    const uint32_t f0 = e4m3x2_to_f16x2(lds16(ks + r0 * kRowScales + 2 * t4));
+    const uint32_t f1 = e4m3x2_to_f16x2(lds16(ks + r1 * kRowScales + 2 * t4));
+    const uint32_t sc0[2] = {__byte_perm(f0, 0, 0x1010), __byte_perm(f0, 0, 0x3232)};
+    const uint32_t sc1[2] = {__byte_perm(f1, 0, 0x1010), __byte_perm(f1, 0, 0x3232)};
     const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
     const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
@@ -238,19 +207,20 @@ __device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n,
       const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
       x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
       y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
-      mma_f16_16816(acc[0], x0, y0, x1, y1, bq[2 * w][0], bq[2 * w][1]);
-      mma_f16_16816(acc[1], x2, y2, x3, y3, bq[2 * w + 1][0], bq[2 * w + 1][1]);
+      mma_f16_16816(acc, x0, y0, x1, y1, bq[2 * w][0], bq[2 * w][1]);
+      mma_f16_16816(acc, x2, y2, x3, y3, bq[2 * w + 1][0], bq[2 * w + 1][1]);
     }
     const int j0 = n * kBlock + r0, j1 = j0 + 8;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[mq][e] = (acc[0][e] + acc[1][e]) * scale_log2;
+    for (int e = 0; e < 4; ++e) x[mq][e] = acc[e];
     if (recent) {
       if (j0 > pos) x[mq][0] = x[mq][1] = -INFINITY;
       if (j1 > pos) x[mq][2] = x[mq][3] = -INFINITY;
     }
   }
 
-  // ---- online softmax per head column (2*t4 + e)
+  // ---- online softmax per head column (2*t4 + e), in the exp2 domain: logit * scale_log2
+  // (the scale is positive, so the maximum of the raw logits scales to the running maximum)
   float p[2][4], alpha[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
@@ -258,15 +228,15 @@ __device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n,
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float m_new = fmaxf(m_run[e], mx);
+    const float m_new = fmaxf(m_run[e], mx * scale_log2);
     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    alpha[e] = exp2f(m_run[e] - m_use);
+    alpha[e] = exp2_ftz(m_run[e] - m_use);
     m_run[e] = m_new;
     float sum = 0.f;
 #pragma unroll
     for (int mq = 0; mq < 2; ++mq) {
-      p[mq][e] = exp2f(x[mq][e] - m_use);
-      p[mq][e + 2] = exp2f(x[mq][e + 2] - m_use);
+      p[mq][e] = exp2_ftz(fmaf(x[mq][e], scale_log2, -m_use));
+      p[mq][e + 2] = exp2_ftz(fmaf(x[mq][e + 2], scale_log2, -m_use));
       sum += p[mq][e] + p[mq][e + 2];
     }
     l_run[e] = l_run[e] * alpha[e] + sum;
@@ -287,15 +257,16 @@ __device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n,
   for (int mq = 0; mq < 2; ++mq) {
     const uint32_t b0 = movmatrix_trans(pack_f16x2(p[mq][0], p[mq][1]));
     const uint32_t b1 = movmatrix_trans(pack_f16x2(p[mq][2], p[mq][3]));
-    const int ka = qk * 32 + mq * 16 + 2 * t4;  // keys ka, ka+1, ka+8, ka+9
+    // k-indices 2t4, 2t4+1, 2t4+8, 2t4+9 are keys pi(.) = t4, t4+4, t4+8, t4+12 of the tile
+    const int ka = qk * 32 + mq * 16 + t4;
     const uint2 va = lds64(vd + ka * kRowBytes + 8 * gq);
-    const uint2 vb = lds64(vd + (ka + 1) * kRowBytes + 8 * gq);
+    const uint2 vb = lds64(vd + (ka + 4) * kRowBytes + 8 * gq);
     const uint2 vc = lds64(vd + (ka + 8) * kRowBytes + 8 * gq);
-    const uint2 ve = lds64(vd + (ka + 9) * kRowBytes + 8 * gq);
+    const uint2 ve = lds64(vd + (ka + 12) * kRowBytes + 8 * gq);
     const uint32_t sab = e4m3x2_to_f16x2(lds8(vs + ka * kRowScales + gq) |
-                                         (lds8(vs + (ka + 1) * kRowScales + gq) << 8));
+                                         (lds8(vs + (ka + 4) * kRowScales + gq) << 8));
     const uint32_t scd = e4m3x2_to_f16x2(lds8(vs + (ka + 8) * kRowScales + gq) |
-                                         (lds8(vs + (ka + 9) * kRowScales + gq) << 8));
+                                         (lds8(vs + (ka + 12) * kRowScales + gq) << 8));
 #pragma unroll
     for (int hw = 0; hw < 2; ++hw) {
       const uint32_t wa = hw ? va.y : va.x, wb = hw ? vb.y : vb.x;
@@ -356,32 +327,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
   if (warp >= kAW) {
     grid_dependency_wait();
     grid_dependents_launch();  // the merge kernel may be scheduled as SMs free up
-    // ---- producer of team `tm`: its items in order, each into the next slot once the
-    // team's four warps have released it
+    // ---- producer of team `tm`: row by row over its entries, an item per entry with a
+    // page (a marker for a row segment with none), then the end item
     const int tm = warp - kAW;
     const int tt = blockIdx.x * kTeams + tm;
     TeamBars* tb = tbars + tm;
-    TeamProd st;
-    st.x0 = range_lo(E, tt, NT);
-    st.nk = range_lo(E, tt + 1, NT) - st.x0;
-    st.pk = 0;
-    st.pb = -1;
-    st.produced = 0;
-    st.seg_any = false;
-    st.end_sent = false;
-    bool failed = false;
-    while (!st.end_sent) {
-      const int slot = st.produced % kTSl;
-      if (st.produced >= kTSl && !mbar_wait_warp(&tb->empty[slot], ((st.produced / kTSl) - 1) & 1)) {
-        failed = true;
-        break;
+    uint8_t* slots = smem + static_cast<size_t>(tm) * kTSl * kSlotBytes;
+    ItemMeta* my_meta = meta + tm * kTSl;
+    const int x0 = range_lo(E, tt, NT), x1 = range_lo(E, tt + 1, NT);
+    int produced = 0;
+    bool ok = true;
+    for (int R = x0 / kTopK; x0 < x1 && R <= (x1 - 1) / kTopK && ok; ++R) {
+      int blk, page, pos;
+      row_pages(a, R, lane, blk, page, pos);
+      const int j0 = max(x0 - R * kTopK, 0), j1 = min(x1 - R * kTopK, kTopK);
+      bool any = false;
+      for (int j = j0; j < j1 && ok; ++j) {
+        const int pj = __shfl_sync(0xffffffffu, page, j), bj = __shfl_sync(0xffffffffu, blk, j);
+        if (pj < 0) continue;
+        any = true;
+        ok = send_item(a, produced, slots, my_meta, tb, lane, R, bj, pj, pos);
       }
-      produce_one(a, st, smem + static_cast<size_t>(tm) * kTSl * kSlotBytes, meta + tm * kTSl, tb, lane);
+      if (ok && !any) ok = send_item(a, produced, slots, my_meta, tb, lane, R, -1, -1, -1);
     }
-    if (failed) {
+    if (ok) ok = send_item(a, produced, slots, my_meta, tb, lane, -1, -1, -1, -1);
+    if (!ok) {
       if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
       // wait (bounded) for the copies still in flight before leaving
-      for (int k = max(0, st.produced - kTSl); k < st.produced; ++k) mbar_wait(&tb->full[k % kTSl], (k / kTSl) & 1);
+      for (int k = max(0, produced - kTSl); k < produced; ++k) mbar_wait(&tb->full[k % kTSl], (k / kTSl) & 1);
     }
     return;
   }

@@ -143,21 +143,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of one phase (for a thread that polls several barriers).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n"
-      "}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait on one phase; false if it gave up (the caller flags MSA_DEVERR_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i)
@@ -166,7 +151,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // The same, called by a whole warp; the verdict is made warp-uniform so that the warp's
-// later shuffles never diverge.
+// later shuffles never diverge.  (Every lane waits: a variant where lane 0 alone polls and
+// broadcasts was measured slower, its divergent loop costing more than the shared polls.)
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   const bool ok = mbar_wait(bar, parity);
   return __all_sync(0xffffffffu, ok) != 0;
