@@ -125,10 +125,18 @@ __device__ __forceinline__ bool send_item(const AttnArgs& a, int& produced, uint
       const int64_t pg = static_cast<int64_t>(page) * a.groups + row % a.groups;
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, kSlotBytes);
-      bulk_g2s(dst, a.k_data + pg * kPageData, kPageData, bar);
-      bulk_g2s(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar);
-      bulk_g2s(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar);
-      bulk_g2s(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar);
+      if (a.q_len == 1) {  // one token per sequence: every page is read once per call
+        const uint64_t pol = l2_evict_first_policy();
+        bulk_g2s_hint(dst, a.k_data + pg * kPageData, kPageData, bar, pol);
+        bulk_g2s_hint(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar, pol);
+        bulk_g2s_hint(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar, pol);
+        bulk_g2s_hint(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar, pol);
+      } else {  // the tokens of a sequence share most pages: keep them in L2
+        bulk_g2s(dst, a.k_data + pg * kPageData, kPageData, bar);
+        bulk_g2s(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar);
+        bulk_g2s(dst + kPageData + kPageScale, a.v_data + pg * kPageData, kPageData, bar);
+        bulk_g2s(dst + 2 * kPageData + kPageScale, a.v_scale + pg * kPageScale, kPageScale, bar);
+      }
     } else {
       mbar_arrive(bar);
     }

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
   // (and its memory) before touching global memory
   grid_dependency_wait();
   grid_dependents_launch();
+  const uint64_t l2_once = l2_evict_first_policy();  // every page is read once per call
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -204,8 +205,8 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, kStageBytes);
         uint8_t* dst = my_stages + stage * kStageBytes;
-        bulk_g2s(dst, a.idx_data + static_cast<int64_t>(page) * kPageData, kPageData, bar);
-        bulk_g2s(dst + kPageData, a.idx_scale + static_cast<int64_t>(page) * kPageScale, kPageScale, bar);
+        bulk_g2s_hint(dst, a.idx_data + static_cast<int64_t>(page) * kPageData, kPageData, bar, l2_once);
+        bulk_g2s_hint(dst + kPageData, a.idx_scale + static_cast<int64_t>(page) * kPageScale, kPageScale, bar, l2_once);
       } else {
         flag_error(a.err, MSA_DEVERR_BAD_PAGE);
         mbar_arrive(bar);
@@ -388,6 +389,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
 
   grid_dependency_wait();
   grid_dependents_launch();
+  const uint64_t l2_once = l2_evict_first_policy();  // every page is read once per call
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int T = a.q_len, G = a.groups;
@@ -432,9 +434,10 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
         uint8_t* dst = my_stages + stage * kHalfBytes;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, kHalfBytes);
-        bulk_g2s(dst, a.idx_data + static_cast<int64_t>(page) * kPageData + ihalf * kHalfData, kHalfData, bar);
-        bulk_g2s(dst + kHalfData, a.idx_scale + static_cast<int64_t>(page) * kPageScale + ihalf * kHalfScale,
-                 kHalfScale, bar);
+        bulk_g2s_hint(dst, a.idx_data + static_cast<int64_t>(page) * kPageData + ihalf * kHalfData, kHalfData, bar,
+                      l2_once);
+        bulk_g2s_hint(dst + kHalfData, a.idx_scale + static_cast<int64_t>(page) * kPageScale + ihalf * kHalfScale,
+                      kHalfScale, bar, l2_once);
       } else {
         if (ihalf == 0) flag_error(a.err, MSA_DEVERR_BAD_PAGE);
         mbar_arrive(bar);
