@@ -144,6 +144,32 @@ __device__ __forceinline__ void score_tile(const uint8_t* st, const uint8_t* ss,
   }
 }
 
+// single-accumulator tile for one n-tile; scales converted once per row pair
+__device__ __forceinline__ void score_tile1(const uint8_t* st, const uint8_t* ss, int r0, int t4,
+                                            const uint32_t (&bq)[1][8][2], float (&acc)[4]) {
+  const int r1 = r0 + 8;
+  const uint4 d0 = lds128(st + r0 * kRowBytes + 16 * t4);
+  const uint4 d1 = lds128(st + r1 * kRowBytes + 16 * t4);
+  const uint32_t f0 = e4m3x2_to_f16x2(lds16(ss + r0 * kRowScales + 2 * t4));
+  const uint32_t f1 = e4m3x2_to_f16x2(lds16(ss + r1 * kRowScales + 2 * t4));
+  const uint32_t sc0[2] = {__byte_perm(f0, 0, 0x1010), __byte_perm(f0, 0, 0x3232)};
+  const uint32_t sc1[2] = {__byte_perm(f1, 0, 0x1010), __byte_perm(f1, 0, 0x3232)};
+  const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
+  const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
+  acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+    e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
+    e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
+    const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
+    x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
+    y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
+    mma_f16_16816(acc, x0, y0, x1, y1, bq[0][2 * w][0], bq[0][2 * w][1]);
+    mma_f16_16816(acc, x2, y2, x3, y3, bq[0][2 * w + 1][0], bq[0][2 * w + 1][1]);
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const IndexerArgs a) {
   // key tiles processed together: enough independent MMA chains per warp
@@ -445,11 +471,11 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
     }
     ihalf ^= 1;
   };
-  const int64_t nhalves = 2 * (u1 - u0);
-  int64_t issued = 0;
+  const int nhalves = static_cast<int>(2 * (u1 - u0));  // per-warp counters fit 32 bits
+  int issued = 0;
   if (u0 < u1) {
     lookup_next();
-    for (; issued < kHStages && issued < nhalves; ++issued) issue_next(static_cast<int>(issued % kHStages));
+    for (; issued < kHStages && issued < nhalves; ++issued) issue_next(issued % kHStages);
   }
 
   // ---- consumer
@@ -457,7 +483,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
   int cur_b = -1, L = 0, posc[2] = {-1, -1};
   PageCursor cc;
   cc.init(prefix, a.batch, u0, u1);
-  int64_t consumed = 0;
+  int consumed = 0;
   bool timed_out = false;
   for (int64_t u = u0; u < u1 && !timed_out; ++u) {
     cc.u = u;
@@ -495,7 +521,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
     bool page_ok = true;
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
-      const int stage = static_cast<int>(consumed % kHStages);
+      const int stage = consumed % kHStages;
       if (!mbar_wait_warp(&my_bars[stage], static_cast<uint32_t>((consumed / kHStages) & 1))) {
         timed_out = true;
         break;
@@ -503,14 +529,14 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
       page_ok = page_ok && ((valid_bits >> stage) & 1u);
       const uint8_t* st = my_stages + stage * kHalfBytes;
       if (page_ok) {
-        float acc[4][1][2][4];
+        float acc[4][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) score_tile<1>(st, st + kHalfData, k * 16 + g, t4, bq, acc[k]);
+        for (int k = 0; k < 4; ++k) score_tile1(st, st + kHalfData, k * 16 + g, t4, bq, acc[k]);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           float v[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] = acc[k][0][0][e] + acc[k][0][1][e];
+          for (int e = 0; e < 4; ++e) v[e] = acc[k][e];
           if (need_mask) {
             const int j0 = n * kBlock + h * 64 + k * 16 + g, j1 = j0 + 8;
             if (j0 > posc[0]) v[0] = -INFINITY;
@@ -525,7 +551,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
       __syncwarp();
       ++consumed;
       if (issued < nhalves) {
-        issue_next(static_cast<int>(issued % kHStages));
+        issue_next(issued % kHStages);
         ++issued;
       }
     }
@@ -552,7 +578,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
 
   if (timed_out) {
     if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
-    for (int64_t k = consumed; k < issued; ++k)
+    for (int k = consumed; k < issued; ++k)
       mbar_wait(&my_bars[k % kHStages], static_cast<uint32_t>((k / kHStages) & 1));
   }
 
