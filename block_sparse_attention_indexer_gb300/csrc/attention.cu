@@ -145,15 +145,38 @@ __device__ __forceinline__ bool send_item(const AttnArgs& a, int& produced, uint
   return true;
 }
 
-// The producer's view of one row: its selection (lane j < 16: block id of entry j) and the
-// page of each entry (-1: empty, past the recent block, or a bad block-table entry).
-__device__ __forceinline__ void row_pages(const AttnArgs& a, int R, int lane, int& blk, int& page, int& pos) {
-  const RowInfo ri = row_info(a, R);
-  blk = (ri.ok && lane < kTopK) ? a.selection[static_cast<int64_t>(R) * kTopK + lane] : -1;
+// The producer's view of one row, in two steps so that a row's loads can be in flight while
+// the row before it is being sent: row_fetch issues the loads that depend only on the row
+// (its selection, lane j < 16: block id of entry j, and its sequence length), row_resolve
+// then checks them and looks up the page of each entry (-1: empty, past the recent block,
+// or a bad block-table entry).
+struct RowRaw {
+  int blk, L;
+};
+
+__device__ __forceinline__ RowRaw row_fetch(const AttnArgs& a, int R, int lane) {
+  RowRaw raw;
+  raw.blk = lane < kTopK ? a.selection[static_cast<int64_t>(R) * kTopK + lane] : -1;
+  raw.L = a.seq_lens[static_cast<unsigned>(R) / static_cast<unsigned>(a.q_len * a.groups)];
+  return raw;
+}
+
+__device__ __forceinline__ void row_resolve(const AttnArgs& a, int R, const RowRaw& raw, int lane, int& blk,
+                                            int& page, int& pos) {
+  const unsigned TG = static_cast<unsigned>(a.q_len * a.groups);
+  const int b = static_cast<int>(static_cast<unsigned>(R) / TG);
+  const int t = static_cast<int>((static_cast<unsigned>(R) - static_cast<unsigned>(b) * TG) /
+                                 static_cast<unsigned>(a.groups));
+  const int L = raw.L;
+  const bool ok = L > 0 && L >= a.q_len && L <= static_cast<int64_t>(a.max_blocks) * kBlock;
+  pos = L - a.q_len + t;
+  const int r = ok ? pos / kBlock : -1;
+  blk = ok ? raw.blk : -1;
+  // the table lookup only needs an in-range block id; its validity comes from ok and r
+  int p = -1;
+  if (blk >= 0 && blk < a.max_blocks) p = a.block_table[static_cast<int64_t>(b) * a.max_blocks + blk];
   page = -1;
-  pos = ri.L - a.q_len + ri.t;
-  if (lane < kTopK && ri.ok && blk >= 0 && blk <= ri.r) {
-    const int p = a.block_table[static_cast<int64_t>(ri.b) * a.max_blocks + blk];
+  if (blk >= 0 && blk <= r) {
     if (p >= 0 && p < a.num_pages)
       page = p;
     else
@@ -345,9 +368,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
     const int x0 = range_lo(E, tt, NT), x1 = range_lo(E, tt + 1, NT);
     int produced = 0;
     bool ok = true;
-    for (int R = x0 / kTopK; x0 < x1 && R <= (x1 - 1) / kTopK && ok; ++R) {
+    const int R_last = (x1 - 1) / kTopK;
+    RowRaw raw = {};
+    if (x0 < x1) raw = row_fetch(a, x0 / kTopK, lane);
+    for (int R = x0 / kTopK; x0 < x1 && R <= R_last && ok; ++R) {
+      RowRaw next = {};
+      if (R < R_last) next = row_fetch(a, R + 1, lane);  // in flight while row R is sent
       int blk, page, pos;
-      row_pages(a, R, lane, blk, page, pos);
+      row_resolve(a, R, raw, lane, blk, page, pos);
+      raw = next;
       const int j0 = max(x0 - R * kTopK, 0), j1 = min(x1 - R * kTopK, kTopK);
       bool any = false;
       for (int j = j0; j < j1 && ok; ++j) {
