@@ -18,6 +18,10 @@ function restates one step of the method as the pages define it:
     ("MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署", §MSA 机制细节);
   * selection per query token and KV group, then sparse GQA equal to dense attention
     restricted to the selected set (same page, §Prefill 执行, steps 2-4);
+  * configuration variants the pages name: the block-score reduction is max or
+    log-sum-exp by model configuration (same page, §Prefill 执行 step 2); init_blocks
+    leading and local_blocks trailing blocks are kept by rule, the rest come from the top-k
+    of the indexer scores, none counted twice (same page, §MSA 机制细节);
   * speculative tokens flattened request-major, each with its own causal position
     (same page, §Decode Kernel 中的投机解码);
   * decode context parallelism: local top-16 per shard, merged exactly by the owner
@@ -71,9 +75,22 @@ def query_positions(length: int, q_len: int) -> np.ndarray:
 # --------------------------------------------------------------------------------------
 # stage 1: indexer score + block max-pool
 # --------------------------------------------------------------------------------------
+def pool_block(values: np.ndarray, pooling: str, axis: int) -> np.ndarray:
+    """One score per block from its keys' scores (-inf = not visible): their maximum, or
+    their log-sum-exp ln(sum_j e^{s_j}) (natural log); -inf for a block with no visible key."""
+    m = values.max(axis=axis)
+    if pooling == "max":
+        return m
+    assert pooling == "lse", pooling
+    mk = np.expand_dims(np.where(np.isfinite(m), m, 0.0), axis)
+    with np.errstate(divide="ignore"):
+        return np.where(np.isfinite(m), np.squeeze(mk, axis) + np.log(np.exp(values - mk).sum(axis=axis)), m)
+
+
 def block_scores(qi_codes, idx_data, idx_scale, block_table, seq_lens, max_blocks: int | None = None,
-                 rows_per_matmul: int = 256, tokens=None, sequences=None) -> np.ndarray:
-    """Block scores S[b, t, g, n] = max over visible keys j of block n of qi[b,t,g] . k_j.
+                 rows_per_matmul: int = 256, tokens=None, sequences=None, pooling: str = "max") -> np.ndarray:
+    """Block scores S[b, t, g, n] = pool over visible keys j of block n of qi[b,t,g] . k_j,
+    pool = max (the recipe) or log-sum-exp.
 
     qi_codes: uint8 E4M3 [B, T, G, Di].  A block with no visible key scores -inf (every
     block after the query's own block, and every block past the sequence end).
@@ -103,7 +120,7 @@ def block_scores(qi_codes, idx_data, idx_scale, block_table, seq_lens, max_block
             j = np.arange(nb * BLOCK)[:, None]
             visible = j <= pos_all[ts][None, :]                       # [nb*128, len(ts)]
             padded = np.where(visible[:, :, None], padded, -np.inf)
-            pooled = padded.reshape(nb, BLOCK, len(ts), G).max(axis=1)   # [nb, len(ts), G]
+            pooled = pool_block(padded.reshape(nb, BLOCK, len(ts), G), pooling, axis=1)  # [nb, len(ts), G]
             out[b, ts, :, :nb] = pooled.transpose(1, 2, 0)
     return out
 
@@ -119,18 +136,24 @@ def rank_key(score: float, n: int):
     return (0, -score, n)
 
 
-def select_row(scores_row: np.ndarray, pos: int, top_k: int = TOP_K) -> np.ndarray:
-    """Selected logical blocks of one (query token, KV group): the recent block
-    r = pos // 128 plus the top-(k-1) of the blocks before it; ascending; -1 padded."""
+def select_row(scores_row: np.ndarray, pos: int, top_k: int = TOP_K, init_blocks: int = 0,
+               local_blocks: int = 1) -> np.ndarray:
+    """Selected logical blocks of one (query token, KV group), min(top_k, r + 1) of them with
+    r = pos // 128 the recent block: the first init_blocks blocks and the last local_blocks
+    blocks up to r are kept by rule (each once), and the remaining places go to the best of
+    the other blocks up to r; ascending; -1 padded.  The recipe (init 0, local 1) is the
+    recent block plus the top-(k-1) of the blocks before it."""
+    assert init_blocks + local_blocks <= top_k
     r = pos // BLOCK
-    cands = sorted(range(r), key=lambda n: rank_key(float(scores_row[n]), n))
-    chosen = sorted(cands[: top_k - 1] + [r])
+    forced = set(range(min(init_blocks, r + 1))) | set(range(max(0, r - local_blocks + 1), r + 1))
+    cands = sorted((n for n in range(r + 1) if n not in forced), key=lambda n: rank_key(float(scores_row[n]), n))
+    chosen = sorted(forced | set(cands[: max(0, top_k - len(forced))]))
     out = np.full(top_k, -1, dtype=np.int32)
     out[: len(chosen)] = chosen
     return out
 
 
-def select_blocks(scores, seq_lens, top_k: int = TOP_K) -> np.ndarray:
+def select_blocks(scores, seq_lens, top_k: int = TOP_K, init_blocks: int = 0, local_blocks: int = 1) -> np.ndarray:
     """sel[b, t, g, :] for every row; scores [B, T, G, max_blocks]."""
     B, T, G, _ = scores.shape
     sel = np.full((B, T, G, top_k), -1, dtype=np.int32)
@@ -140,7 +163,7 @@ def select_blocks(scores, seq_lens, top_k: int = TOP_K) -> np.ndarray:
             continue
         for t, pos in enumerate(query_positions(L, T)):
             for g in range(G):
-                sel[b, t, g] = select_row(scores[b, t, g], int(pos), top_k)
+                sel[b, t, g] = select_row(scores[b, t, g], int(pos), top_k, init_blocks, local_blocks)
     return sel
 
 
@@ -217,12 +240,12 @@ def dense_causal_attention(q_codes, k_data, k_scale, v_data, v_scale, block_tabl
 
 
 def msa_decode(q_codes, qi_codes, cache, block_table, seq_lens, heads_per_group: int,
-               top_k: int = TOP_K):
+               top_k: int = TOP_K, init_blocks: int = 0, local_blocks: int = 1, pooling: str = "max"):
     """The whole decode step: scores -> selection -> attention.
     cache = (k_data, k_scale, v_data, v_scale, idx_data, idx_scale)."""
     k_data, k_scale, v_data, v_scale, idx_data, idx_scale = cache
-    s = block_scores(qi_codes, idx_data, idx_scale, block_table, seq_lens)
-    sel = select_blocks(s, seq_lens, top_k)
+    s = block_scores(qi_codes, idx_data, idx_scale, block_table, seq_lens, pooling=pooling)
+    sel = select_blocks(s, seq_lens, top_k, init_blocks, local_blocks)
     out, lse = sparse_attention(q_codes, k_data, k_scale, v_data, v_scale, block_table, seq_lens, sel,
                                 heads_per_group)
     return s, sel, out, lse

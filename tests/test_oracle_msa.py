@@ -299,3 +299,88 @@ def test_dcp_merge_is_exact():
         cuts = np.linspace(0, nb, shards + 1).astype(int)
         lists = [M.dcp_local_candidates(row, pos, int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:])]
         assert np.array_equal(M.dcp_merge(lists, pos), M.select_row(row, pos))
+
+
+# ------------------------------------------------------------------ configuration variants
+# (block rules: "MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署", §MSA 机制细节 for init /
+# local blocks, §Prefill 执行 step 2 for the max or log-sum-exp block reduction)
+def _variant_bruteforce(scores_row, r, k, init_blocks, local_blocks):
+    """Forced blocks (the first init_blocks and the last local_blocks up to r, each once)
+    plus, among every subset of the other blocks up to r of the remaining size, the one with
+    the largest score sum, ties to the lexicographically smallest."""
+    forced = set(range(min(init_blocks, r + 1))) | set(range(max(0, r - local_blocks + 1), r + 1))
+    others = [n for n in range(r + 1) if n not in forced]
+    m = min(max(0, k - len(forced)), len(others))
+    best = None
+    for sub in itertools.combinations(others, m):
+        tot = sum(scores_row[n] for n in sub)
+        if best is None or tot > best[0] or (tot == best[0] and sub < best[1]):
+            best = (tot, sub)
+    return sorted(forced | set(best[1]))
+
+
+def test_select_variants_equal_subset_bruteforce():
+    rng = np.random.default_rng(17)
+    for trial in range(400):
+        k = int(rng.integers(1, 7))
+        init = int(rng.integers(0, k + 1))
+        local = int(rng.integers(0, k - init + 1))
+        r = int(rng.integers(0, 11))
+        row = rng.integers(-3, 4, size=12).astype(np.float64)   # many exact ties
+        got = M.select_row(row, r * 128 + int(rng.integers(0, 128)), top_k=k, init_blocks=init, local_blocks=local)
+        want = _variant_bruteforce(row, r, k, init, local)
+        assert [int(x) for x in got if x >= 0] == want, (k, init, local, r)
+        assert len(want) == min(k, r + 1)
+        assert (got[len(want):] == -1).all()
+
+
+def test_select_recipe_is_the_default_variant():
+    rng = np.random.default_rng(23)
+    for _ in range(100):
+        row = rng.standard_normal(40)
+        pos = int(rng.integers(0, 40 * 128))
+        assert np.array_equal(M.select_row(row, pos), M.select_row(row, pos, 16, 0, 1))
+
+
+def test_lse_pooling_equals_library_logsumexp_of_exact_scores():
+    from scipy.special import logsumexp
+    w, cache, table, lens, q, qi = small_case([300, 130], q_len=2, hg=1, seed=29)
+    s = M.block_scores(qi, cache[4], cache[5], table, lens, pooling="lse")
+    _, _, _, _, idx_data, idx_scale = cache
+    for b in range(2):
+        L = int(lens[b])
+        keys = np.concatenate([F.nvfp4_dequantize(idx_data[table[b, n]], idx_scale[table[b, n]])
+                               for n in range(-(-L // 128))])[:L]
+        for t in range(2):
+            pos = L - 2 + t
+            for g in range(4):
+                qv = F.e4m3_decode(qi[b, t, g])
+                for n in range(-(-L // 128)):
+                    js = [j for j in range(n * 128, min((n + 1) * 128, L)) if j <= pos]
+                    if not js:
+                        assert s[b, t, g, n] == -np.inf
+                        continue
+                    want = logsumexp([float(qv @ keys[j]) for j in js])
+                    assert abs(s[b, t, g, n] - want) <= 1e-9 * max(1.0, abs(want))
+
+
+def test_lse_pooling_closed_forms():
+    w, cache, table, lens, q, qi = small_case([300], q_len=1, seed=31)
+    idx_data, idx_scale = cache[4], cache[5]
+    for n in range(3):                                # every key of each block = its key 5
+        page = table[0, n]
+        idx_data[page] = idx_data[page, 5]
+        idx_scale[page] = idx_scale[page, 5]
+    s_max = M.block_scores(qi, idx_data, idx_scale, table, lens)
+    s_lse = M.block_scores(qi, idx_data, idx_scale, table, lens, pooling="lse")
+    pos = 299                                         # blocks 0, 1 full; block 2 holds 44 keys
+    for g in range(4):
+        for n, count in [(0, 128), (1, 128), (2, pos - 256 + 1)]:
+            assert s_lse[0, 0, g, n] == pytest.approx(s_max[0, 0, g, n] + math.log(count), rel=1e-12, abs=1e-12)
+    # in general: max <= lse <= max + ln(visible keys)
+    w, cache, table, lens, q, qi = small_case([700, 260], q_len=3, seed=37)
+    a = M.block_scores(qi, cache[4], cache[5], table, lens)
+    l = M.block_scores(qi, cache[4], cache[5], table, lens, pooling="lse")
+    fin = np.isfinite(a)
+    assert np.array_equal(fin, np.isfinite(l))
+    assert (l[fin] >= a[fin] - 1e-12).all() and (l[fin] <= a[fin] + math.log(128) + 1e-12).all()
