@@ -12,6 +12,8 @@ from .binding import (  # noqa: F401
     MSA_OP_INDEXER_SCORES,
     MSA_OP_SELECT_BLOCKS,
     MSA_OP_SPARSE_ATTN,
+    MSA_SCORE_LSE,
+    MSA_SCORE_MAX,
     Batch,
     Config,
     MsaError,

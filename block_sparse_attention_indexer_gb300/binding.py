@@ -29,13 +29,14 @@ _lib = ctypes.CDLL(LIB_PATH)
 MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUDA = range(5)
 MSA_OP_INDEXER_SCORES, MSA_OP_SELECT_BLOCKS, MSA_OP_SPARSE_ATTN, MSA_OP_DECODE = range(4)
 MSA_DEVERR_BAD_PAGE, MSA_DEVERR_BAD_SEQLEN, MSA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+MSA_SCORE_MAX, MSA_SCORE_LSE = 0, 1
 
 
 class _Config(ctypes.Structure):
     _fields_ = [("num_kv_groups", ctypes.c_int32), ("heads_per_group", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("index_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("init_blocks", ctypes.c_int32), ("local_blocks", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("score_type", ctypes.c_int32)]
 
 
 class _Cache(ctypes.Structure):
@@ -117,11 +118,12 @@ class Config:
     init_blocks: int = 0
     local_blocks: int = 1
     softmax_scale: float = 0.0      # 0 = 1/sqrt(head_dim)
+    score_type: int = 0             # MSA_SCORE_MAX (0) or MSA_SCORE_LSE (1)
 
     def c(self):
         return ctypes.byref(_Config(self.num_kv_groups, self.heads_per_group, self.head_dim, self.index_dim,
                                     self.block_size, self.top_k, self.init_blocks, self.local_blocks,
-                                    self.softmax_scale))
+                                    self.softmax_scale, self.score_type))
 
     @property
     def num_heads(self):

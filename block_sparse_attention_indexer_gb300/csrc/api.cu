@@ -24,9 +24,11 @@ msa_status_t check_config(const msa_config_t* c) {
   if (c == nullptr) return MSA_ERR_INVALID_ARG;
   if (c->num_kv_groups < 1 || c->num_kv_groups > 8 || c->heads_per_group < 1 || c->heads_per_group > 8)
     return MSA_ERR_UNSUPPORTED;
-  if (c->head_dim != 128 || c->index_dim != 128 || c->block_size != 128 || c->top_k != 16 || c->init_blocks != 0 ||
-      c->local_blocks != 1)
+  if (c->head_dim != 128 || c->index_dim != 128 || c->block_size != 128) return MSA_ERR_UNSUPPORTED;
+  if (c->top_k < 1 || c->top_k > kSelTopK || c->init_blocks < 0 || c->local_blocks < 0 ||
+      c->init_blocks + c->local_blocks > c->top_k)
     return MSA_ERR_UNSUPPORTED;
+  if (c->score_type != MSA_SCORE_MAX && c->score_type != MSA_SCORE_LSE) return MSA_ERR_UNSUPPORTED;
   if (!(c->softmax_scale >= 0.0f) || !std::isfinite(c->softmax_scale)) return MSA_ERR_INVALID_ARG;
   return MSA_OK;
 }
@@ -105,6 +107,7 @@ IndexerArgs indexer_args(const msa_config_t* cfg, const msa_cache_t* cache, cons
   a.index_q = index_q;
   a.block_scores = scores;
   a.err = err;
+  a.lse = cfg->score_type == MSA_SCORE_LSE ? 1 : 0;
   return a;
 }
 
@@ -117,6 +120,9 @@ SelectArgs select_args(const msa_config_t* cfg, const msa_batch_t* batch, const 
   a.q_len = batch->q_len;
   a.groups = cfg->num_kv_groups;
   a.selection = sel;
+  a.top_k = cfg->top_k;
+  a.init_blocks = cfg->init_blocks;
+  a.local_blocks = cfg->local_blocks;
   return a;
 }
 

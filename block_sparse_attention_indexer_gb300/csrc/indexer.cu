@@ -170,7 +170,7 @@ __device__ __forceinline__ void score_tile1(const uint8_t* st, const uint8_t* ss
   }
 }
 
-template <int NT>
+template <int NT, bool LSE>
 __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const IndexerArgs a) {
   // key tiles processed together: enough independent MMA chains per warp
   constexpr int MG = NT == 1 ? 4 : (NT == 2 ? 2 : 1);
@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
   grid_dependency_wait();
   grid_dependents_launch();
   const uint64_t l2_once = l2_evict_first_policy();  // every page is read once per call
+  constexpr bool lse = LSE;                             // block pooling: log-sum-exp or max
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -279,8 +280,12 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
       const int rows = tc * G;
       const int pos_min = L - T + t0, pos_max = pos_min + tc - 1;
       float mx[NT][2];
+      PoolState pl[NT][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = -INFINITY;
+      for (int nt = 0; nt < NT; ++nt) {
+        mx[nt][0] = mx[nt][1] = -INFINITY;
+        pl[nt][0] = pl[nt][1] = {-INFINITY, 0.f};
+      }
 
       if (page_ok && n * kBlock <= pos_max) {
         if (b != cur_b || c != cur_c) {
@@ -341,8 +346,8 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              mx[nt][0] = fmaxf(mx[nt][0], fmaxf(v[nt][0], v[nt][2]));
-              mx[nt][1] = fmaxf(mx[nt][1], fmaxf(v[nt][1], v[nt][3]));
+              pool_add(pl[nt][0], v[nt][0], v[nt][2], lse);
+              pool_add(pl[nt][1], v[nt][1], v[nt][3], lse);
             }
           }
         }
@@ -350,11 +355,10 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const Indexe
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float v = mx[nt][e];
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-            mx[nt][e] = v;
+            pool_merge_xor(pl[nt][e], 4, lse);
+            pool_merge_xor(pl[nt][e], 8, lse);
+            pool_merge_xor(pl[nt][e], 16, lse);
+            mx[nt][e] = pool_result(pl[nt][e], lse);
           }
       }
       if (g == 0) {
@@ -406,6 +410,7 @@ constexpr int kHalfData = kPageData / 2;    // 4096
 constexpr int kHalfScale = kPageScale / 2;  // 512
 constexpr int kHalfBytes = kHalfData + kHalfScale;
 
+template <bool LSE>
 __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const IndexerArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
@@ -416,6 +421,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
   grid_dependency_wait();
   grid_dependents_launch();
   const uint64_t l2_once = l2_evict_first_policy();  // every page is read once per call
+  constexpr bool lse = LSE;                             // block pooling: log-sum-exp or max
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int T = a.q_len, G = a.groups;
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
     }
     const int pos_min = L - T;
     const bool need_mask = (n + 1) * kBlock - 1 > pos_min;
-    float mx[2] = {-INFINITY, -INFINITY};
+    PoolState pl[2] = {{-INFINITY, 0.f}, {-INFINITY, 0.f}};
     bool page_ok = true;
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
@@ -544,8 +550,8 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
             if (j1 > posc[0]) v[2] = -INFINITY;
             if (j1 > posc[1]) v[3] = -INFINITY;
           }
-          mx[0] = fmaxf(mx[0], fmaxf(v[0], v[2]));
-          mx[1] = fmaxf(mx[1], fmaxf(v[1], v[3]));
+          pool_add(pl[0], v[0], v[2], lse);
+          pool_add(pl[1], v[1], v[3], lse);
         }
       }
       __syncwarp();
@@ -556,13 +562,14 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
       }
     }
     if (timed_out) break;
+    float mx[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float v = page_ok ? mx[e] : -INFINITY;
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      mx[e] = v;
+      if (!page_ok) pl[e] = {-INFINITY, 0.f};
+      pool_merge_xor(pl[e], 4, lse);
+      pool_merge_xor(pl[e], 8, lse);
+      pool_merge_xor(pl[e], 16, lse);
+      mx[e] = pool_result(pl[e], lse);
     }
     if (g == 0) {
 #pragma unroll
@@ -592,10 +599,11 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
   }
 }
 
-static cudaError_t launch_half(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+template <bool LSE>
+static cudaError_t launch_half_t(const IndexerArgs& a, int num_sms, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(kHWarps) * kHStages * kHalfBytes + kHWarps * kHStages * sizeof(uint64_t) +
                       (a.batch + 1) * sizeof(int32_t);
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(indexer_half_kernel), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(indexer_half_kernel<LSE>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
@@ -607,16 +615,20 @@ static cudaError_t launch_half(const IndexerArgs& a, int num_sms, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, indexer_half_kernel, a);
+  e = cudaLaunchKernelEx(&cfg, indexer_half_kernel<LSE>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int NT>
-static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+static cudaError_t launch_half(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+  return a.lse ? launch_half_t<true>(a, num_sms, s) : launch_half_t<false>(a, num_sms, s);
+}
+
+template <int NT, bool LSE>
+static cudaError_t launch_nt_t(const IndexerArgs& a, int num_sms, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(kIdxWarps) * kIdxStages * kStageBytes +
                       kIdxWarps * kIdxStages * sizeof(uint64_t) + (a.batch + 1) * sizeof(int32_t);
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(indexer_kernel<NT>), smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(indexer_kernel<NT, LSE>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
@@ -628,9 +640,14 @@ static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, indexer_kernel<NT>, a);
+  e = cudaLaunchKernelEx(&cfg, indexer_kernel<NT, LSE>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int NT>
+static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+  return a.lse ? launch_nt_t<NT, true>(a, num_sms, s) : launch_nt_t<NT, false>(a, num_sms, s);
 }
 
 cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s) {

@@ -213,6 +213,36 @@ __device__ __forceinline__ uint32_t lds8(const void* p) {
   return v;
 }
 
+// Block pooling of key scores into one score per block ("MiniMax M3 x vLLM：百万 token 多模态推理的
+// Day-0 部署", §Prefill 执行 step 2: a block-level rule such as max or log-sum-exp).  The running
+// state of one column: the maximum m and, for log-sum-exp, s = sum over the values seen of
+// e^{x - m}; -inf values (keys not visible) count as absent.  lse is warp-uniform.
+struct PoolState {
+  float m, s;
+};
+
+__device__ __forceinline__ void pool_add(PoolState& p, float a, float b, bool lse) {
+  const float mn = fmaxf(p.m, fmaxf(a, b));
+  if (lse && mn != -INFINITY) p.s = p.s * expf(p.m - mn) + expf(a - mn) + expf(b - mn);
+  p.m = mn;
+}
+
+// Combines the states of lanes lane and lane ^ mask (all 32 lanes call it).
+__device__ __forceinline__ void pool_merge_xor(PoolState& p, int mask, bool lse) {
+  const float mo = __shfl_xor_sync(0xffffffffu, p.m, mask);
+  const float mn = fmaxf(p.m, mo);
+  if (lse) {
+    const float so = __shfl_xor_sync(0xffffffffu, p.s, mask);
+    if (mn != -INFINITY) p.s = p.s * expf(p.m - mn) + so * expf(mo - mn);
+  }
+  p.m = mn;
+}
+
+// The block score: m, or m + ln s (natural log); -inf for a block with no visible key.
+__device__ __forceinline__ float pool_result(const PoolState& p, bool lse) {
+  return (lse && p.m != -INFINITY) ? p.m + logf(p.s) : p.m;
+}
+
 // Order of float scores as unsigned integers: larger float -> larger key, -0 == +0,
 // NaN below -inf.
 __device__ __forceinline__ uint32_t score_order(float f) {

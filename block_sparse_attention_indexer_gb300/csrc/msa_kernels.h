@@ -18,6 +18,7 @@ struct IndexerArgs {
   const uint8_t* index_q;      // [B][T][G][128] E4M3
   float* block_scores;         // [B][T][G][max_blocks]
   uint32_t* err;
+  int32_t lse;                 // block pooling: 0 max, 1 log-sum-exp
 };
 
 struct SelectArgs {
@@ -25,6 +26,7 @@ struct SelectArgs {
   const int32_t* seq_lens;
   int32_t batch, max_blocks, q_len, groups;
   int32_t* selection;          // [B][T][G][16]
+  int32_t top_k, init_blocks, local_blocks;
   int32_t row_cap;             // candidates per row staged in shared memory (set by the launcher)
 };
 

@@ -94,6 +94,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+template <bool LSE>
 __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const IndexerArgs a, int tiles_per_seq) {
   extern __shared__ uint8_t smem_raw[];
   grid_dependency_wait();
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
       const int r = warp * 32 + lane;
       const bool row_ok = r < nrows;
       const int pos = row_ok ? L - T + (row0 + r) / G : -1;
+      constexpr bool lse = LSE;  // block pooling: log-sum-exp or max
       for (int k = 0; k < nblk; ++k) {
         const int acc = k & 1;
         if (!mbar_wait_warp(&sh->acc_full[acc], (k / 2) & 1)) {
@@ -315,6 +317,22 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
             for (int j = 0; j < 32; ++j)
               if (j0 + c0 + j <= pos) mx = fmaxf(mx, __uint_as_float(v[j]));
           }
+        }
+        if (lse) {
+          // log-sum-exp pooling: a second pass over the accumulator, sum e^{s - max} (the
+          // warp-collective loads run in every lane; a row with nothing visible stays -inf)
+          const float m_use = mx == -INFINITY ? 0.f : mx;
+          float sum = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < kBlock; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kBlock + c0, v);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j0 + c0 + j <= pos) sum += expf(__uint_as_float(v[j]) - m_use);
+          }
+          if (mx != -INFINITY) mx += logf(sum);
         }
         tc_fence_before();
         __syncwarp();
@@ -343,11 +361,12 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
   if (warp == 9 && nblk > 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
 }
 
-cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s) {
+template <bool LSE>
+static cudaError_t launch_prefill_t(const IndexerArgs& a, cudaStream_t s) {
   const int rows_seq = a.q_len * a.groups;
   const int tiles_per_seq = (rows_seq + kPfRows - 1) / kPfRows;
   const int ranges = (a.max_blocks + kPfKb - 1) / kPfKb;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_indexer_kernel), kPfSmem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_indexer_kernel<LSE>), kPfSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -359,9 +378,13 @@ cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, prefill_indexer_kernel, a, tiles_per_seq);
+  e = cudaLaunchKernelEx(&cfg, prefill_indexer_kernel<LSE>, a, tiles_per_seq);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s) {
+  return a.lse ? launch_prefill_t<true>(a, s) : launch_prefill_t<false>(a, s);
 }
 
 }  // namespace msa

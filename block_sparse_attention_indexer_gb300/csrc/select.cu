@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs
     return;
   }
   const int r = (L - a.q_len + t) / kBlock;
-  const int id = select_row_warp(a.block_scores + row * a.max_blocks, r, lane,
+  const int id = select_row_warp(a.block_scores + row * a.max_blocks, r, a.top_k, a.init_blocks, a.local_blocks, lane,
                                  sord_all + static_cast<int64_t>(warp) * a.row_cap, a.row_cap, buf[warp], kSelCap);
   if (lane < kTopK) out[lane] = id;
 }

@@ -1,28 +1,28 @@
-// Top-k block selection of one row by one warp, with the most recent block forced; used by
-// the selection kernel and, on the fused decode path, by the attention kernel's producers.
+// Top-k block selection of one row by one warp, with forced blocks; used by the selection
+// kernel.
 //
 // Attention runs only over the top-16 blocks, the most recent block always among them
 // ("vLLM liefert Day-0-Unterstützung für MiniMax-M3.1-Flash", §MSA-Grundlagen): the recent
 // block r = pos / 128 is kept and counted inside the 16 (local_blocks = 1, init_blocks = 0,
 // the local block not counted twice: "MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署",
-// §MSA 机制细节); the other 15 are the best blocks before r.  Ranking: higher score first,
+// §MSA 机制细节, which also names init_blocks leading and local_blocks trailing blocks as
+// configuration); the other places go to the best blocks.  Ranking: higher score first,
 // equal scores to the lower block index, NaN below -inf.  Output ascending, -1 padded.
 //
-// Every candidate n < r gets the 64-bit key  order(score) << 32 | (0xffffffff - n)  (all
-// keys distinct, larger = better).
+// Every candidate n gets the 64-bit key  order(score) << 32 | (0xffffffff - n)  (all keys
+// distinct, larger = better).  For W winners:
 //   1. each lane takes the largest score order (32-bit, without the index) of its strided
-//      share (held in registers for rows of up to 1,024 candidates); the 15th largest lane
-//      maximum is a lower bound of the 15th best candidate (15 lanes each hold one at least
-//      that large);
-//   2. the candidates at or above that bound (at least 15, about 20 for the workloads'
-//      score distributions) are compacted to shared memory as their exact 64-bit keys:
-//      per-lane counts, a warp prefix sum, and every lane writes its own;
+//      share (held in registers for up to 1,024 candidates); the W-th largest lane maximum
+//      is a lower bound of the W-th best candidate (W lanes each hold one at least that
+//      large);
+//   2. the candidates at or above that bound (at least W, about 20 for W = 15 and the
+//      workloads' score distributions) are compacted to shared memory as their exact
+//      64-bit keys: per-lane counts, a warp prefix sum, and every lane writes its own;
 //   3. if at most 32 survive (the usual case) each survivor's rank comes from 32 pairwise
-//      comparisons across the warp, and each of the 15 winners takes its place in
-//      ascending block order (the recent block r, larger than every candidate, goes last);
-//      otherwise 15 rounds of warp arg-max pick the winners, over the compacted survivors
-//      or, if they overflowed the buffer (adversarial score layouts), over the whole row,
-//      and a bitonic sort orders the 16 ids.
+//      comparisons across the warp, and each winner takes its place in ascending block
+//      order; otherwise W rounds of warp arg-max pick the winners, over the compacted
+//      survivors or, if they overflowed the buffer (adversarial score layouts), over all
+//      candidates, and a bitonic sort orders them.
 #pragma once
 
 #include "msa_device.cuh"
@@ -95,67 +95,68 @@ __device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v, int lane) {
   return v;
 }
 
-// Selection of one row with recent block r: returns, in lane i < 16, the i-th selected block
-// id in ascending order (-1 past min(16, r + 1)).  s: the row's block scores (global);
-// sord: optional shared staging of row_cap score orders for rows longer than 1,024
-// candidates (else they are re-read from L2); cb: a shared buffer of cap >= 32 survivor keys.
-// All 32 lanes call it together.
-__device__ __forceinline__ int select_row_warp(const float* s, int r, int lane, uint32_t* sord, int row_cap,
-                                               uint64_t* cb, int cap) {
-  if (r < kTopK) return (lane < kTopK && lane <= r) ? lane : -1;  // every block 0..r
-  const bool in_regs = r <= 32 * 32;      // candidate orders held in registers
-  const bool staged = !in_regs && sord != nullptr && r <= row_cap;
+// The W best of the candidate blocks lo .. hi-1 of one row (0 <= W <= 16, W < hi - lo):
+// returns, in lane i < W, the i-th winner in ascending block order (-1 in the other lanes).
+// s: the row's block scores (global); sord: optional shared staging of row_cap score orders
+// for more than 1,024 candidates (else they are re-read from L2); cb: a shared buffer of
+// cap >= 32 survivor keys.  All 32 lanes call it together.
+__device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, int W, int lane, uint32_t* sord,
+                                               int row_cap, uint64_t* cb, int cap) {
+  if (W <= 0) return -1;
+  const int nc = hi - lo;                 // candidates
+  const bool in_regs = nc <= 32 * 32;     // candidate orders held in registers
+  const bool staged = !in_regs && sord != nullptr && nc <= row_cap;
 
-  // 1. score orders of the candidates, with the lane maxima; the 15th largest lane maximum
-  //    bounds the winners from below (15 lanes each hold a candidate at least that large)
+  // 1. score orders of the candidates, with the lane maxima; the W-th largest lane maximum
+  //    bounds the winners from below (W lanes each hold a candidate at least that large)
   uint32_t o[32];
   uint32_t lmax = 0;
   if (in_regs) {
     float v[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      const int n = 32 * k + lane;
-      v[k] = n < r ? __ldcg(s + n) : 0.f;
+      const int c = 32 * k + lane;
+      v[k] = c < nc ? __ldcg(s + lo + c) : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      o[k] = (32 * k + lane < r) ? score_order(v[k]) : 0u;
+      o[k] = (32 * k + lane < nc) ? score_order(v[k]) : 0u;
       lmax = max(lmax, o[k]);
     }
   } else {
-    for (int n0 = 0; n0 < r; n0 += 32 * 32) {  // 32 loads in flight per lane
+    for (int c0 = 0; c0 < nc; c0 += 32 * 32) {  // 32 loads in flight per lane
       float v[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const int n = n0 + 32 * k + lane;
-        v[k] = n < r ? __ldcg(s + n) : 0.f;
+        const int c = c0 + 32 * k + lane;
+        v[k] = c < nc ? __ldcg(s + lo + c) : 0.f;
       }
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const int n = n0 + 32 * k + lane;
-        if (n < r) {
+        const int c = c0 + 32 * k + lane;
+        if (c < nc) {
           const uint32_t ord = score_order(v[k]);
-          if (staged) sord[n] = ord;
+          if (staged) sord[c] = ord;
           lmax = max(lmax, ord);
         }
       }
     }
   }
-  const uint32_t bound = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lmax, lane), kTopK - 2);
+  const uint32_t bound = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lmax, lane), W - 1);
   __syncwarp();
-  auto order_of = [&](int n) -> uint32_t { return staged ? sord[n] : score_order(__ldcg(s + n)); };
+  auto order_of = [&](int c) -> uint32_t { return staged ? sord[c] : score_order(__ldcg(s + lo + c)); };
   auto key_of = [](uint32_t ord, int n) -> uint64_t {
     return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(n));
   };
 
-  // 2. compact the candidates whose order is >= bound (at least 15) as exact 64-bit keys:
+  // 2. compact the candidates whose order is >= bound (at least W) as exact 64-bit keys:
   //    per-lane counts, a warp prefix sum, then every lane writes its own at its offset
   int cnt = 0;
   if (in_regs) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) cnt += (32 * k + lane < r && o[k] >= bound) ? 1 : 0;
+    for (int k = 0; k < 32; ++k) cnt += (32 * k + lane < nc && o[k] >= bound) ? 1 : 0;
   } else {
-    for (int n = lane; n < r; n += 32) cnt += order_of(n) >= bound ? 1 : 0;
+    for (int c = lane; c < nc; c += 32) cnt += order_of(c) >= bound ? 1 : 0;
   }
   int incl = cnt;
 #pragma unroll
@@ -169,27 +170,27 @@ __device__ __forceinline__ int select_row_warp(const float* s, int r, int lane, 
     if (in_regs) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const int n = 32 * k + lane;
-        if (n < r && o[k] >= bound) cb[idx++] = key_of(o[k], n);
+        const int c = 32 * k + lane;
+        if (c < nc && o[k] >= bound) cb[idx++] = key_of(o[k], lo + c);
       }
     } else {
-      for (int n = lane; n < r; n += 32) {
-        const uint32_t ord = order_of(n);
-        if (ord >= bound) cb[idx++] = key_of(ord, n);
+      for (int c = lane; c < nc; c += 32) {
+        const uint32_t ord = order_of(c);
+        if (ord >= bound) cb[idx++] = key_of(ord, lo + c);
       }
     }
   }
   __syncwarp();
 
-  // 3. the 15 winners, written in ascending block order, then the recent block
+  // 3. the W winners in ascending block order
   if (count <= 32) {
     // rank of each survivor by key (keys are distinct; empty lanes hold 0, below every key),
-    // then each winner's position among the winners by block index: r is larger than all
+    // then each winner's position among the winners by block index
     const uint64_t k = lane < count ? cb[lane] : 0ull;
     int rank = 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) rank += shfl_u64(k, j) > k ? 1 : 0;
-    const bool win = lane < count && rank < kTopK - 1;
+    const bool win = lane < count && rank < W;
     const int id = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k));
     const uint32_t wm = __ballot_sync(0xffffffffu, win);
     int at = 0;
@@ -201,17 +202,16 @@ __device__ __forceinline__ int select_row_warp(const float* s, int r, int lane, 
     __syncwarp();  // every survivor key is read: the buffer now takes the ids
     int* ids = reinterpret_cast<int*>(cb);
     if (win) ids[at] = id;
-    if (lane == 0) ids[kTopK - 1] = r;
     __syncwarp();
-    const int out = lane < kTopK ? ids[lane] : -1;
+    const int out = lane < W ? ids[lane] : -1;
     __syncwarp();
     return out;
   }
-  int mine = -1;  // lane i (< 15) holds the block of the i-th winner
+  int mine = 0x7fffffff;  // lane i (< W) holds the block of the i-th winner by rank
   {
     const bool overflow = count > cap;
     uint64_t prev = ~0ull;
-    for (int round = 0; round < kTopK - 1; ++round) {
+    for (int round = 0; round < W; ++round) {
       uint64_t best = 0;
       if (!overflow) {
         for (int i = lane; i < count; i += 32) {
@@ -221,13 +221,13 @@ __device__ __forceinline__ int select_row_warp(const float* s, int r, int lane, 
       } else if (in_regs) {  // the survivors overflowed the buffer: scan the whole row
 #pragma unroll
         for (int kk = 0; kk < 32; ++kk) {
-          const int n = 32 * kk + lane;
-          const uint64_t k = n < r ? key_of(o[kk], n) : 0ull;
+          const int c = 32 * kk + lane;
+          const uint64_t k = c < nc ? key_of(o[kk], lo + c) : 0ull;
           if (k < prev && k > best) best = k;
         }
       } else {
-        for (int n = lane; n < r; n += 32) {
-          const uint64_t k = key_of(order_of(n), n);
+        for (int c = lane; c < nc; c += 32) {
+          const uint64_t k = key_of(order_of(c), lo + c);
           if (k < prev && k > best) best = k;
         }
       }
@@ -236,11 +236,29 @@ __device__ __forceinline__ int select_row_warp(const float* s, int r, int lane, 
       if (lane == round) mine = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best));
     }
   }
-  if (lane == kTopK - 1) mine = r;
-  // 4. ascending order of the 16 ids (the other lanes carry INT_MAX)
-  const int sorted_id = warp_sort_asc_i32(lane < kTopK ? mine : 0x7fffffff, lane);
-  return lane < kTopK ? sorted_id : -1;
+  // 4. ascending order of the W ids (the other lanes carry INT_MAX)
+  const int sorted_id = warp_sort_asc_i32(mine, lane);
+  return lane < W ? sorted_id : -1;
 }
 
+// The selection of one row whose recent block is r: min(top_k, r + 1) blocks in ascending
+// order -- the first init_blocks, the best top_k - init_blocks - local_blocks of the blocks
+// between them and the local window, and the last local_blocks up to r (init_blocks +
+// local_blocks <= top_k <= 16; with r + 1 <= top_k every block 0 .. r).  Lane i < 16 gets
+// the i-th id (-1 past the end).  The recipe (top_k 16, init 0, local 1) is r plus the 15
+// best blocks before it.
+__device__ __forceinline__ int select_row_warp(const float* s, int r, int top_k, int init_blocks, int local_blocks,
+                                               int lane, uint32_t* sord, int row_cap, uint64_t* cb, int cap) {
+  if (r + 1 <= top_k) return (lane < kTopK && lane <= r) ? lane : -1;
+  // here r >= top_k, so the init blocks, the candidates and the local window are disjoint
+  // and in that order: [0, I) [I, r - Lc + 1) [r - Lc + 1, r]
+  const int W = top_k - init_blocks - local_blocks;
+  const int win = top_blocks_warp(s, init_blocks, r - local_blocks + 1, W, lane, sord, row_cap, cb, cap);
+  const int from_win = __shfl_sync(0xffffffffu, win, (lane - init_blocks) & 31);
+  if (lane < init_blocks) return lane;
+  if (lane < init_blocks + W) return from_win;
+  if (lane < top_k) return r - local_blocks + 1 + (lane - init_blocks - W);
+  return -1;
+}
 
 }  // namespace msa

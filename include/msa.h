@@ -42,7 +42,8 @@
  *   queries q        uint8 E4M3 [batch][q_len][G*Hg][D]   (head h belongs to group h / Hg)
  *   index queries    uint8 E4M3 [batch][q_len][G][Di]
  *   block_scores     float [batch][q_len][G][max_blocks]
- *   selection        int32 [batch][q_len][G][top_k]  ascending logical block ids, -1 padded
+ *   selection        int32 [batch][q_len][G][16]  ascending logical block ids, -1 padded (rows
+ *                    are 16 wide, the largest top_k; entries past min(top_k, r + 1) are -1)
  *   out              bfloat16 bits (uint16) [batch][q_len][G*Hg][D]
  *   lse              float [batch][q_len][G*Hg]  natural log of the softmax denominator
  */
@@ -56,7 +57,7 @@
 extern "C" {
 #endif
 
-#define MSA_ABI_VERSION 1
+#define MSA_ABI_VERSION 2
 
 typedef enum {
   MSA_OK = 0,
@@ -71,11 +72,22 @@ typedef enum {
 #define MSA_DEVERR_BAD_SEQLEN 0x2u  /* seq_len < q_len (but > 0), or > max_blocks*128 */
 #define MSA_DEVERR_TIMEOUT 0x4u     /* a bounded wait inside a kernel gave up */
 
+/* Block-score reduction over the visible keys of a block ("MiniMax M3 x vLLM：百万 token
+ * 多模态推理的 Day-0 部署", §Prefill 执行 step 2: a block-level rule such as max or
+ * log-sum-exp, by model configuration). */
+#define MSA_SCORE_MAX 0  /* max_j s_j (the recipe) */
+#define MSA_SCORE_LSE 1  /* ln sum_j e^{s_j} (natural log) */
+
 /* Sparse configuration.  The pages' M3 recipe: block 128, top-16, init_blocks = 0,
- * local_blocks = 1 ("MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署", §MSA 机制细节).
- * This build implements exactly: num_kv_groups in 1..8, heads_per_group in 1..8,
- * head_dim = index_dim = block_size = 128, top_k = 16, init_blocks = 0, local_blocks = 1;
- * anything else returns MSA_ERR_UNSUPPORTED. */
+ * local_blocks = 1, max pooling ("MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署",
+ * §MSA 机制细节, which names init_blocks / local_blocks as configuration).
+ * This build implements: num_kv_groups in 1..8, heads_per_group in 1..8,
+ * head_dim = index_dim = block_size = 128, 1 <= top_k <= 16, init_blocks >= 0,
+ * local_blocks >= 0 with init_blocks + local_blocks <= top_k, score_type MSA_SCORE_MAX or
+ * MSA_SCORE_LSE; anything else returns MSA_ERR_UNSUPPORTED.
+ * Selection of a row whose recent block is r = pos / 128: min(top_k, r + 1) blocks -- the
+ * first init_blocks blocks and the last local_blocks blocks up to r (each once), and the
+ * best of the other blocks up to r for the remaining places. */
 typedef struct {
   int32_t num_kv_groups;    /* G */
   int32_t heads_per_group;  /* Hg */
@@ -86,6 +98,7 @@ typedef struct {
   int32_t init_blocks;      /* leading blocks always kept */
   int32_t local_blocks;     /* trailing (recent) blocks always kept */
   float softmax_scale;      /* logits = (q . k) * softmax_scale; 0 means 1/sqrt(head_dim) */
+  int32_t score_type;       /* MSA_SCORE_MAX or MSA_SCORE_LSE */
 } msa_config_t;
 
 /* The paged NVFP4 caches (device, caller-owned, read-only for decode). */
@@ -145,9 +158,10 @@ msa_status_t msa_nvfp4_insert(const float* x, int64_t n_tokens, int32_t rows_per
 /* FP8 E4M3 encoding of float32 values (round to nearest even, saturating at +-448, sign kept). */
 msa_status_t msa_fp8_quantize(const float* x, int64_t n, uint8_t* out, void* stream);
 
-/* Stage 1 -- indexer score + block max-pool.
- * block_scores[b][t][g][n] = max over visible keys j of block n of (qi[b][t][g] . key_j),
- * exact products (E2M1 x E4M3 x E4M3) accumulated in float32; -inf where block n has no
+/* Stage 1 -- indexer score + block pooling.
+ * block_scores[b][t][g][n] = max (MSA_SCORE_MAX) or log-sum-exp (MSA_SCORE_LSE) over the
+ * visible keys j of block n of (qi[b][t][g] . key_j), exact products (E2M1 x E4M3 x E4M3)
+ * accumulated in float32 (the log-sum-exp with expf / logf); -inf where block n has no
  * visible key (n beyond the query's own block or past the sequence end).  Entries
  * n >= ceil(seq_len/128) are written -inf too.  Any q_len works; q_len <= 8 takes the
  * decode kernel, larger q_len the prefill kernel.
@@ -156,11 +170,12 @@ msa_status_t msa_indexer_scores(const msa_config_t* cfg, const msa_cache_t* cach
                                 const uint8_t* index_q, float* block_scores, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
-/* Stage 2 -- top-k block selection with the recent block forced.
- * For each (b, t, g): r = pos / 128 is always selected; the other top_k - 1 come from the
- * blocks n < r ranked by (score descending, index ascending; NaN below -inf); the
- * result is sorted ascending, min(top_k, r + 1) ids, -1 padded.  Bit-exact for given
- * scores.  No workspace. */
+/* Stage 2 -- top-k block selection with forced blocks.
+ * For each (b, t, g) with recent block r = pos / 128: the first init_blocks and the last
+ * local_blocks blocks up to r are always selected (the recipe: r alone); the other places,
+ * up to min(top_k, r + 1) in all, go to the blocks between them ranked by (score
+ * descending, index ascending; NaN below -inf); the result is sorted ascending, -1 padded
+ * to 16.  Bit-exact for given scores.  No workspace. */
 msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch, const float* block_scores,
                                int32_t* selection, void* stream);
 

@@ -71,8 +71,11 @@ def test_workspace_sizes(lib):
     # unsupported configurations report 0
     bad = b._Config(4, 8, 64, 128, 128, 16, 0, 1, 0.0)
     assert f(b.MSA_OP_DECODE, ctypes.byref(bad), ctypes.byref(bt)) == 0
-    bad = b._Config(4, 8, 128, 128, 128, 16, 1, 1, 0.0)
+    bad = b._Config(4, 8, 128, 128, 128, 4, 3, 2, 0.0)      # init + local > top_k
     assert f(b.MSA_OP_DECODE, ctypes.byref(bad), ctypes.byref(bt)) == 0
+    # the configuration variants are accepted: top_k 8 with init 2 and local 2, log-sum-exp
+    var = b._Config(4, 8, 128, 128, 128, 8, 2, 2, 0.0, b.MSA_SCORE_LSE)
+    assert f(b.MSA_OP_DECODE, ctypes.byref(var), ctypes.byref(bt)) > 0
 
 
 def test_validation_rejects_before_any_cuda_call(lib):
@@ -83,8 +86,9 @@ def test_validation_rejects_before_any_cuda_call(lib):
     cache = b._Cache(16, 16, 16, 16, 16, 16, 10)
     batch = b._Batch(16, 16, 2, 8, 1)
     ref = ctypes.byref
-    # unsupported sparse configs (top_k 8, local_blocks 2, 9 groups)
-    for cfg in [b._Config(4, 8, 128, 128, 128, 8, 0, 1, 0.0), b._Config(4, 8, 128, 128, 128, 16, 0, 2, 0.0),
+    # unsupported sparse configs (top_k 17, top_k 0, init + local > top_k, score type 2, 9 groups)
+    for cfg in [b._Config(4, 8, 128, 128, 128, 17, 0, 1, 0.0), b._Config(4, 8, 128, 128, 128, 0, 0, 0, 0.0),
+                b._Config(4, 8, 128, 128, 128, 8, 4, 5, 0.0), b._Config(4, 8, 128, 128, 128, 16, 0, 1, 0.0, 2),
                 b._Config(9, 8, 128, 128, 128, 16, 0, 1, 0.0)]:
         assert L.msa_decode(ref(cfg), ref(cache), ref(batch), 16, 16, 16, None, None, 16, 1 << 30, None) == 2
     # null / misaligned pointers, bad sizes

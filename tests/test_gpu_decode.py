@@ -147,7 +147,7 @@ def test_host_validation_rejects_before_launch():
     small = torch.zeros(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(msa.MsaError, match="WORKSPACE"):
         msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, None, None, small)
-    bad_cfg = msa.Config(heads_per_group=8, top_k=8)
+    bad_cfg = msa.Config(heads_per_group=8, top_k=17)
     ws = msa.alloc_workspace(msa.MSA_OP_DECODE, dw.cfg, dw.batch)
     with pytest.raises(msa.MsaError, match="UNSUPPORTED"):
         msa.msa_decode(bad_cfg, dw.cache, dw.batch, dw.q, dw.qi, out, None, None, ws)
