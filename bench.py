@@ -416,7 +416,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16 mma (exact nvfp4/fp8 products), f32 acc", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "operands": "NVFP4 cache and FP8 queries widened exactly to f16", "data": "synthetic",
         "config": {"workload": w.name, "batch": B, "q_len": T, "heads": H, "kv_groups": 4, "head_dim": 128,
                    "index_dim": 128, "top_k": 16, "block": 128, "mean_ctx": float(np.mean(dw.lens)),
                    "tokens_in_cache": int(np.sum(dw.lens)), "l2": "flushed between timed steps (512 MiB write)",
