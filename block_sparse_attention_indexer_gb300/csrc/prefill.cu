@@ -11,13 +11,15 @@
 //   * a CTA owns one tile of 128 query rows and a range of 32 key blocks; the query tile is
 //     converted once (FP8 E4M3 -> f16, exact) into a K-major, 128-byte-swizzled shared
 //     tile, the A operand of every MMA of the CTA;
-//   * warp roles: warp 8 streams the raw NVFP4 pages (9 KB) with bulk async copies into a
-//     3-stage ring; warps 4-7 dequantise each page exactly into f16 (cvt e2m1x2 -> f16x2 times
-//     the f16 block scale) in the same swizzled K-major layout (B operand, 2 stages); one
-//     thread of warp 9 issues tcgen05.mma (M = 128 rows, N = 128 keys, K = 16, eight per
-//     block) into one of two 128-column TMEM accumulators; warps 0-3 read the accumulator
-//     back with tcgen05.ld (one TMEM lane quarter each), apply the causal mask and max-pool
-//     the 128 columns into the block's score;
+//   * warp roles: warp 12 streams the raw NVFP4 pages (9 KB) with bulk async copies into a
+//     3-stage ring; warps 4-11 dequantise each page exactly into f16 (cvt e2m1x2 -> f16x2
+//     times the f16 block scale) in the same swizzled K-major layout (B operand, 2 stages) --
+//     two warps per scheduler, two independent items each per page, since one warp per
+//     scheduler left the conversion latency-bound; one thread of warp 13 issues tcgen05.mma
+//     (M = 128 rows, N = 128 keys, K = 16, eight per block) into one of two 128-column TMEM
+//     accumulators; warps 0-3 convert the query tile while the first pages arrive, then read
+//     the accumulator back with tcgen05.ld (one TMEM lane quarter each), apply the causal
+//     mask and max-pool the 128 columns into the block's score;
 //   * every hand-off is an mbarrier (tcgen05.commit arrives on the MMA side), every wait is
 //     bounded; key blocks that no row of the tile can see are never loaded.
 #include <cuda_fp16.h>
@@ -30,7 +32,9 @@ namespace msa {
 constexpr int kPfKb = 32;                 // key blocks per CTA
 constexpr int kPfRawSt = 3;               // raw NVFP4 page stages
 constexpr int kPfKSt = 2;                 // f16 key tile stages
-constexpr int kPfWarps = 10;              // 0-3 epilogue, 4-7 dequant, 8 copies, 9 MMA
+constexpr int kPfWarps = 14;              // 0-3 query tile + epilogue, 4-11 dequant, 12 copies, 13 MMA
+constexpr int kPfDeqWarps = 8;
+constexpr int kPfCopyWarp = 12, kPfMmaWarp = 13;
 constexpr int kPfRows = 128;              // query rows per CTA (MMA M)
 constexpr int kHalfTile = kPfRows * 128;  // one [128 x 64] f16 K-major SW128 tile: 16 KB
 constexpr int kRawBytes = kPageData + kPageScale;
@@ -130,10 +134,10 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
   if (tid == 0) {
     for (int i = 0; i < kPfRawSt; ++i) {
       mbar_init(&sh->raw_full[i], 1);
-      mbar_init(&sh->raw_empty[i], 4);
+      mbar_init(&sh->raw_empty[i], kPfDeqWarps);
     }
     for (int i = 0; i < kPfKSt; ++i) {
-      mbar_init(&sh->k_full[i], 4);
+      mbar_init(&sh->k_full[i], kPfDeqWarps);
       mbar_init(&sh->k_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
     }
     sh->pages[tid] = page;
   }
-  if (warp == 9 && nblk > 0) {
+  if (warp == kPfMmaWarp && nblk > 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(&sh->tmem_base)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
   bool failed = false;
 
   if (nblk > 0) {
-    if (warp == 8) {
+    if (warp == kPfCopyWarp) {
       // ---- raw page producer
       if (lane == 0) {
         for (int k = 0; k < nblk && !failed; ++k) {
@@ -190,31 +194,9 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
         if (failed)
           for (int k = max(0, nblk - kPfRawSt); k < nblk; ++k) mbar_wait(&sh->raw_full[k % kPfRawSt], (k / kPfRawSt) & 1);
       }
-    } else if (warp >= 4 && warp < 8) {
-      // ---- dequantisers: the query tile once, then every key page
+    } else if (warp >= 4 && warp < 4 + kPfDeqWarps) {
+      // ---- dequantisers: every key page, two items per thread per page
       const int dt = tid - 128;
-      for (int item = dt; item < kPfRows * 8; item += 128) {
-        const int r = item >> 3, c = item & 7;  // 16 FP8 query bytes = dims 16c .. 16c+15
-        uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (r < nrows) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              a.index_q + (static_cast<int64_t>(b) * rows_seq + row0 + r) * kDim + 16 * c));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            h[2 * i] = e4m3x2_to_f16x2(w[i]);
-            h[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
-          }
-        }
-        uint8_t* tdst = q_tile + (c < 4 ? 0 : kHalfTile);
-        const int ch = 2 * (c & 3);
-        *reinterpret_cast<uint4*>(tdst + sw128(r, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(tdst + sw128(r, ch + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->q_ready);
-
       for (int k = 0; k < nblk; ++k) {
         const int s = k % kPfRawSt, ks = k % kPfKSt;
         if (!mbar_wait_warp(&sh->raw_full[s], (k / kPfRawSt) & 1) ||
@@ -229,14 +211,24 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
         // c = i >> 1 of row 4 (o >> 1) + (i & 1) + 2 (((i >> 1) & 1) ^ (o & 1)).  An octet's
         // loads then hit 8 distinct 16-byte bank groups (row parity x chunk), and with the chunk
         // order of the upper half of the dims rotated by 2 so do its swizzled stores
-        for (int item = dt; item < kPfRows * 4; item += 128) {
+        constexpr int kItems = kPfRows * 4 / (kPfDeqWarps * 32);
+        int rr[kItems], cc[kItems];
+        uint4 d[kItems];
+        uint32_t sc[kItems];
+#pragma unroll
+        for (int u = 0; u < kItems; ++u) {
+          const int item = dt + u * kPfDeqWarps * 32;
           const int i8 = item & 7, oct = item >> 3;
-          const int r = 4 * (oct >> 1) + (i8 & 1) + 2 * (((i8 >> 1) & 1) ^ (oct & 1));
-          const int c = i8 >> 1;  // dims 32c .. 32c+31
-          const uint4 d = lds128(src + r * kRowBytes + 16 * c);
-          const uint32_t sc = lds16(src + kPageData + r * kRowScales + 2 * c);
-          const uint32_t s0 = e4m3_bcast_f16x2(sc, 0), s1 = e4m3_bcast_f16x2(sc, 1);
-          const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+          rr[u] = 4 * (oct >> 1) + (i8 & 1) + 2 * (((i8 >> 1) & 1) ^ (oct & 1));
+          cc[u] = i8 >> 1;  // dims 32c .. 32c+31
+          d[u] = lds128(src + rr[u] * kRowBytes + 16 * cc[u]);
+          sc[u] = lds16(src + kPageData + rr[u] * kRowScales + 2 * cc[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kItems; ++u) {
+          const int r = rr[u], c = cc[u];
+          const uint32_t s0 = e4m3_bcast_f16x2(sc[u], 0), s1 = e4m3_bcast_f16x2(sc[u], 1);
+          const uint32_t w[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
           uint32_t h[16];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -263,7 +255,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
           mbar_arrive(&sh->raw_empty[s]);
         }
       }
-    } else if (warp == 9) {
+    } else if (warp == kPfMmaWarp) {
       // ---- MMA issuer
       if (lane == 0) {
         const uint32_t idesc = umma_idesc_f16(kPfRows, kBlock);
@@ -289,11 +281,43 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
       }
       __syncwarp();
     } else {
-      // ---- epilogue (warps 0-3 = TMEM lane quarters 0-3): causal max-pool per block
+      // ---- warps 0-3: the query tile (FP8 E4M3 -> f16, exact), all loads issued first
+      {
+        constexpr int kQItems = kPfRows * 8 / 128;
+        uint4 qv[kQItems];
+#pragma unroll
+        for (int u = 0; u < kQItems; ++u) {
+          const int item = tid + 128 * u, r = item >> 3, c = item & 7;  // dims 16c .. 16c+15
+          qv[u] = r < nrows ? __ldg(reinterpret_cast<const uint4*>(
+                                  a.index_q + (static_cast<int64_t>(b) * rows_seq + row0 + r) * kDim + 16 * c))
+                            : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kQItems; ++u) {
+          const int item = tid + 128 * u, r = item >> 3, c = item & 7;
+          const uint32_t w[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            h[2 * i] = e4m3x2_to_f16x2(w[i]);
+            h[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+          }
+          uint8_t* tdst = q_tile + (c < 4 ? 0 : kHalfTile);
+          const int ch = 2 * (c & 3);
+          *reinterpret_cast<uint4*>(tdst + sw128(r, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(tdst + sw128(r, ch + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->q_ready);
+      }
+
+      // ---- epilogue (warps 0-3 = TMEM lane quarters 0-3): causal pooling per block
       const int r = warp * 32 + lane;
       const bool row_ok = r < nrows;
       const int pos = row_ok ? L - T + (row0 + r) / G : -1;
       constexpr bool lse = LSE;  // block pooling: log-sum-exp or max
+      const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
       for (int k = 0; k < nblk; ++k) {
         const int acc = k & 1;
         if (!mbar_wait_warp(&sh->acc_full[acc], (k / 2) & 1)) {
@@ -301,38 +325,41 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
           break;
         }
         tc_fence_after();
-        const int n = n0 + k;
-        const int j0 = n * kBlock;
-        float mx = -INFINITY;
+        const int lim = pos - (n0 + k) * kBlock;  // columns 0 .. lim are visible to this row
+        // max: four independent chains, two 32-column loads in flight per wait
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c0 = 0; c0 < kBlock; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kBlock + c0, v);
+        for (int c0 = 0; c0 < kBlock; c0 += 64) {
+          uint32_t v[2][32];
+          tmem_ld32(trow + acc * kBlock + c0, v[0]);
+          tmem_ld32(trow + acc * kBlock + c0 + 32, v[1]);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (j0 + c0 + 31 <= pos) {
+          if (c0 + 63 <= lim) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+            for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(v[j >> 5][j & 31]));
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j0 + c0 + j <= pos) mx = fmaxf(mx, __uint_as_float(v[j]));
+            for (int j = 0; j < 64; ++j)
+              m4[j & 3] = fmaxf(m4[j & 3], c0 + j <= lim ? __uint_as_float(v[j >> 5][j & 31]) : -INFINITY);
           }
         }
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         if (lse) {
           // log-sum-exp pooling: a second pass over the accumulator, sum e^{s - max} (the
           // warp-collective loads run in every lane; a row with nothing visible stays -inf)
           const float m_use = mx == -INFINITY ? 0.f : mx;
-          float sum = 0.f;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c0 = 0; c0 < kBlock; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kBlock + c0, v);
+          for (int c0 = 0; c0 < kBlock; c0 += 64) {
+            uint32_t v[2][32];
+            tmem_ld32(trow + acc * kBlock + c0, v[0]);
+            tmem_ld32(trow + acc * kBlock + c0 + 32, v[1]);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j0 + c0 + j <= pos) sum += expf(__uint_as_float(v[j]) - m_use);
+            for (int j = 0; j < 64; ++j)
+              if (c0 + j <= lim) s4[j & 3] += expf(__uint_as_float(v[j >> 5][j & 31]) - m_use);
           }
-          if (mx != -INFINITY) mx += logf(sum);
+          if (mx != -INFINITY) mx += logf((s4[0] + s4[1]) + (s4[2] + s4[3]));
         }
         tc_fence_before();
         __syncwarp();
@@ -358,7 +385,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9 && nblk > 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+  if (warp == kPfMmaWarp && nblk > 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
 }
 
 template <bool LSE>
