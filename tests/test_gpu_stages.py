@@ -19,6 +19,7 @@ CASES = [
     ("chunked_t20", [640, 3000], 20, 8, True),               # 80 rows: tcgen05 GEMM indexer
     ("chunked_t12", [1500, 999, 260], 12, 4, True),          # 48 rows: streaming indexer, 2 chunks
     ("prefill_t300", [300, 5000 + 77, 40000], 300, 8, True),  # 1,200 rows: several GEMM row tiles
+    ("prefill_t96", [96, 3000 + 5], 96, 8, True),            # 384 rows: the last CTA has one full tile
     ("hg4_t1", [4096] * 3, 1, 4, False),
     ("many_rows_t4", [300 + 37 * i for i in range(64)], 4, 8, True),     # 1024 rows: no split
     ("rows256_t2", [2500 + 101 * i for i in range(32)], 2, 8, True),      # 256 rows: 4 splits
