@@ -7,6 +7,7 @@
 #include <unordered_map>
 
 #include "../../include/msa.h"
+#include "api_internal.h"
 #include "msa_kernels.h"
 
 using namespace msa;
@@ -76,6 +77,17 @@ size_t sel_bytes(const msa_config_t* c, const msa_batch_t* b) {
   return align_up(static_cast<size_t>(rows_tg(b, c)) * kSelTopK * sizeof(int32_t));
 }
 size_t partial_bytes() { return align_up(attn_partial_bytes()); }
+
+// long query chunks (chunked prefill) attend block-major: their scratch is the K-to-Q plan and
+// one partial state per (token, head, selection slot) instead of the team kernel's slots
+bool block_major(const msa_config_t* c, const msa_batch_t* b) {
+  return bm_supported(b->batch, b->q_len, c->num_kv_groups, c->heads_per_group, b->max_blocks);
+}
+size_t attn_scratch_bytes(const msa_config_t* c, const msa_batch_t* b) {
+  return block_major(c, b)
+             ? align_up(bm_workspace_bytes(b->batch, b->q_len, c->num_kv_groups, c->heads_per_group, b->max_blocks))
+             : partial_bytes();
+}
 
 float scale_log2(const msa_config_t* c) {
   const float sm = c->softmax_scale > 0.0f ? c->softmax_scale : 1.0f / std::sqrt(static_cast<float>(c->head_dim));
@@ -151,7 +163,38 @@ AttnArgs attn_args(const msa_config_t* cfg, const msa_cache_t* cache, const msa_
   return a;
 }
 
+// stage 3: block-major for long query chunks (when allowed), else the persistent team kernel
+cudaError_t run_attention(const msa_config_t* cfg, const msa_batch_t* batch, const AttnArgs& a, uint8_t* scratch,
+                          int sms, cudaStream_t s, bool block_major_ok) {
+  if (block_major_ok && block_major(cfg, batch))
+    return launch_block_major_attention(
+        a, bm_workspace(scratch, batch->batch, batch->q_len, cfg->num_kv_groups, cfg->heads_per_group, batch->max_blocks),
+        sms, s);
+  return launch_attention(a, sms, s);
+}
+
 }  // namespace
+
+size_t msa::team_attn_workspace_bytes() { return kErrBytes + partial_bytes(); }
+
+msa_status_t msa::sparse_attn_entry(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                    const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream, bool block_major_ok) {
+  msa_status_t st;
+  if ((st = check_config(cfg)) != MSA_OK || (st = check_batch(batch)) != MSA_OK ||
+      (st = check_cache(cache, false, true)) != MSA_OK)
+    return st;
+  if (batch->batch == 0) return MSA_OK;
+  if (q == nullptr || selection == nullptr || out == nullptr || !aligned16(q)) return MSA_ERR_INVALID_ARG;
+  const size_t need = block_major_ok ? msa_workspace_bytes(MSA_OP_SPARSE_ATTN, cfg, batch) : team_attn_workspace_bytes();
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MSA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AttnArgs a = attn_args(cfg, cache, batch, q, selection, out, lse, reinterpret_cast<float*>(ws + kErrBytes),
+                         reinterpret_cast<uint32_t*>(ws));
+  return cuda_status(run_attention(cfg, batch, a, ws + kErrBytes, sms, static_cast<cudaStream_t>(stream), block_major_ok));
+}
 
 cudaError_t msa::ensure_dynamic_smem(const void* kernel, size_t bytes) {
   static std::mutex mu;
@@ -188,8 +231,8 @@ size_t msa_workspace_bytes(msa_op_t op, const msa_config_t* cfg, const msa_batch
   switch (op) {
     case MSA_OP_INDEXER_SCORES: return kErrBytes;
     case MSA_OP_SELECT_BLOCKS: return 0;
-    case MSA_OP_SPARSE_ATTN: return kErrBytes + partial_bytes();
-    case MSA_OP_DECODE: return kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch) + partial_bytes();
+    case MSA_OP_SPARSE_ATTN: return kErrBytes + attn_scratch_bytes(cfg, batch);
+    case MSA_OP_DECODE: return kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch) + attn_scratch_bytes(cfg, batch);
   }
   return 0;
 }
@@ -245,21 +288,7 @@ msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch
 msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                                     const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
                                     void* workspace, size_t workspace_bytes, void* stream) {
-  msa_status_t st;
-  if ((st = check_config(cfg)) != MSA_OK || (st = check_batch(batch)) != MSA_OK ||
-      (st = check_cache(cache, false, true)) != MSA_OK)
-    return st;
-  if (batch->batch == 0) return MSA_OK;
-  if (q == nullptr || selection == nullptr || out == nullptr || !aligned16(q)) return MSA_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < msa_workspace_bytes(MSA_OP_SPARSE_ATTN, cfg, batch) ||
-      !aligned16(workspace))
-    return MSA_ERR_WORKSPACE;
-  const int sms = num_sms_of_current_device();
-  if (sms <= 0) return MSA_ERR_CUDA;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* partial = reinterpret_cast<float*>(ws + kErrBytes);
-  AttnArgs a = attn_args(cfg, cache, batch, q, selection, out, lse, partial, reinterpret_cast<uint32_t*>(ws));
-  return cuda_status(launch_attention(a, sms, static_cast<cudaStream_t>(stream)));
+  return msa::sparse_attn_entry(cfg, cache, batch, q, selection, out, lse, workspace, workspace_bytes, stream, true);
 }
 
 msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
@@ -284,12 +313,12 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
   int32_t* sel = selection_out != nullptr
                      ? selection_out
                      : reinterpret_cast<int32_t*>(ws + kErrBytes + scores_bytes(cfg, batch));
-  float* partial = reinterpret_cast<float*>(ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch));
+  uint8_t* scratch = ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch);
   cudaError_t e = run_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
   if (e == cudaSuccess) e = launch_select(select_args(cfg, batch, scores, sel), s);
-  AttnArgs aa = attn_args(cfg, cache, batch, q, sel, out, lse, partial, err);
+  AttnArgs aa = attn_args(cfg, cache, batch, q, sel, out, lse, reinterpret_cast<float*>(scratch), err);
   aa.q_early = 1;  // the kernel before it is this step's selection
-  if (e == cudaSuccess) e = launch_attention(aa, sms, s);
+  if (e == cudaSuccess) e = run_attention(cfg, batch, aa, scratch, sms, s, true);
   return cuda_status(e);
 }
 

@@ -2,6 +2,7 @@
 // kernel translation units.  Host-only declarations; every pointer is device memory.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -74,6 +75,24 @@ cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s);
 constexpr int kPrefillMinRows = 64;
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s);
+
+// KV-block-major attention for long query chunks (chunked prefill): K-to-Q CSR plan, block
+// attention writing one partial state per (token, head, selection slot), log-sum-exp merge.
+struct BmWorkspace {
+  int32_t* off;   // [B][G][max_blocks + 1] CSR offsets of each (sequence, group)
+  int32_t* cnt;   // [B][G][max_blocks] entries per block (zeroed before each plan)
+  int32_t* cur;   // [B][G][max_blocks] insertion cursors
+  int32_t* ent;   // [B][G][T * 16] entries t * 16 + slot, grouped by block
+  float2* pm;     // [B][T][H][16] (m in the scaled log2 domain, l) of each slot; m = -inf: empty
+  __half* po;     // [B][T][H][16][128] o / l of each slot
+  __half* q16;    // [B][T][H][128] the queries in f16
+};
+// query tokens per sequence from which the block-major form is used
+constexpr int kBlockMajorMinTokens = 64;
+bool bm_supported(int64_t batch, int q_len, int groups, int heads_per_group, int max_blocks);
+size_t bm_workspace_bytes(int64_t batch, int q_len, int groups, int heads_per_group, int max_blocks);
+BmWorkspace bm_workspace(void* base, int64_t batch, int q_len, int groups, int heads_per_group, int max_blocks);
+cudaError_t launch_block_major_attention(const AttnArgs& a, const BmWorkspace& w, int num_sms, cudaStream_t s);
 
 // Upper bound of the attention grid (one CTA per SM); the partial-state area is sized for it.
 constexpr int kAttnMaxCtas = 160;

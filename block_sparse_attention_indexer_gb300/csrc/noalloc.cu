@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/msa.h"
+#include "api_internal.h"
 #include "msa_kernels.h"
 
 namespace {
@@ -46,11 +47,13 @@ extern "C" msa_status_t msa_sparse_attn_decode_noalloc(const msa_config_t* cfg, 
                                                        const msa_batch_t* batch, const uint8_t* q,
                                                        const int32_t* selection, uint16_t* out, float* lse,
                                                        void* stream) {
-  const size_t need = msa_workspace_bytes(MSA_OP_SPARSE_ATTN, cfg, batch);
   // 0 means an invalid configuration or batch: the regular entry point names the error
   // (it validates them before it looks at the workspace)
-  if (need == 0) return msa_sparse_attn_decode(cfg, cache, batch, q, selection, out, lse, nullptr, 0, stream);
-  if (need > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // batch too large for the static scratch
+  if (msa_workspace_bytes(MSA_OP_SPARSE_ATTN, cfg, batch) == 0)
+    return msa_sparse_attn_decode(cfg, cache, batch, q, selection, out, lse, nullptr, 0, stream);
+  // this entry point always runs the query-major team kernel, whose scratch does not grow
+  // with the batch
+  if (msa::team_attn_workspace_bytes() > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;
   void* scratch = nullptr;
   msa_status_t st = noalloc_scratch(&scratch);
   if (st != MSA_OK) return st;
@@ -58,5 +61,6 @@ extern "C" msa_status_t msa_sparse_attn_decode_noalloc(const msa_config_t* cfg, 
   // are read
   if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MSA_ERR_CUDA;
-  return msa_sparse_attn_decode(cfg, cache, batch, q, selection, out, lse, scratch, kNoAllocScratchBytes, stream);
+  return msa::sparse_attn_entry(cfg, cache, batch, q, selection, out, lse, scratch, kNoAllocScratchBytes, stream,
+                                false);
 }

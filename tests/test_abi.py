@@ -66,8 +66,28 @@ def test_workspace_sizes(lib):
     assert f(b.MSA_OP_SELECT_BLOCKS, ctypes.byref(cfg), ctypes.byref(bt)) == 0
     assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + partial
     assert f(b.MSA_OP_DECODE, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + scores + sel + partial
-    bt = b._Batch(1, 1, 1, 544, 4096)
+    bt = b._Batch(1, 1, 1, 544, 63)   # 63 query tokens: still the team kernel
     assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + partial
+
+    # from 64 query tokens on (chunked prefill) the attention runs block-major: CSR offsets,
+    # block counts, insertion cursors and entries, (m, l) and o / l in f16 for every
+    # (token, head, selection slot), and the queries in f16, each area rounded up to 256 bytes
+    def al(x):
+        return (x + 255) // 256 * 256
+
+    def block_major(B, T, G, Hg, MB):
+        slots = B * T * G * Hg * 16
+        return (al(B * G * (MB + 1) * 4) + 2 * al(B * G * MB * 4) + al(B * G * T * 16 * 4) + al(slots * 8)
+                + al(slots * 128 * 2) + al(B * T * G * Hg * 128 * 2))
+
+    bt = b._Batch(1, 1, 1, 544, 4096)
+    bm = block_major(1, 4096, 4, 8, 544)
+    assert bm == 8960 + 2 * 8704 + 1048576 + 16777216 + 536870912 + 33554432
+    assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + bm
+    assert f(b.MSA_OP_DECODE, ctypes.byref(cfg), ctypes.byref(bt)) == (
+        256 + al(4096 * 4 * 544 * 4) + al(4096 * 4 * 16 * 4) + bm)
+    bt = b._Batch(1, 1, 2, 300, 64)
+    assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + block_major(2, 64, 4, 8, 300)
     # unsupported configurations report 0
     bad = b._Config(4, 8, 64, 128, 128, 16, 0, 1, 0.0)
     assert f(b.MSA_OP_DECODE, ctypes.byref(bad), ctypes.byref(bt)) == 0
