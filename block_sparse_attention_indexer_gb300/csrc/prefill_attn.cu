@@ -158,7 +158,6 @@ struct TcShared {
   uint64_t raw_full, kv_full, kv_free;
   uint64_t q_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
   uint32_t tmem_base;
-  int2 meta[4][kBmRows];  // per tile (mod 4) and row: partial-state index (-1: no row), last visible key
 };
 // K | V^T | Q[2] | P[2] | raw page | shared
 constexpr size_t kTcSmem = 1024 + 6 * static_cast<size_t>(kTcTile) + kBmPageBytes + sizeof(TcShared);
@@ -305,7 +304,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
     }
     fence_mbar_init();
   }
-  for (int i = tid; i < 4 * kBmRows; i += kTcThreads) (&sh->meta[0][0])[i] = make_int2(-1, -1);
   if (warp == kTcMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh->tmem_base)),
                  "r"(kTcTmemCols));
@@ -338,10 +336,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
     if (u < units && lt == 0) issue_page(u);
     int nunit = 0, tile = 0;
     bool pending = u < units;  // a page copy is in flight
+    // thread lt gathers row lt of every tile: (token slot lt / Hg, head lt % Hg)
+    const int tl = lt / Hg, hh = lt % Hg;
+    const bool has_row = tl < tok_per_tile;  // (with 128 % Hg != 0 the last rows are unused)
     for (; u < units && !failed; ++nunit) {
-      const int bg = static_cast<int>(u / MB), n = static_cast<int>(u % MB), b = bg / G, g = bg % G;
-      const int L = a.seq_lens[b];
-      // dequantise once the previous unit's products are done with K and V^T
+      const int bg = static_cast<int>(u / MB), b = bg / G, g = bg % G;
+      const int32_t* ent = w.ent + static_cast<int64_t>(bg) * E;
+      const int nt = (e1 - e0 + tok_per_tile - 1) / tok_per_tile;
+      // query tile j of the unit (global tile `tile`) with its row metadata
+      auto gather = [&](int j) -> bool {
+        const int bb = tile & 1, e = e0 + j * tok_per_tile;
+        const int et = (has_row && e + tl < e1) ? ent[e + tl] : -1;
+        if (tile >= 2 && !mbar_wait(&sh->q_empty[bb], ((tile >> 1) - 1) & 1)) return false;
+        if (et >= 0) {
+          const int64_t qrow = (static_cast<int64_t>(b) * T + (et >> 4)) * H + g * Hg + hh;
+          const __half* src = w.q16 + qrow * kDim;
+          const uint32_t q = smem_u32(qt + bb * kTcTile);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) cp_async16(q + (c >> 3) * kTcHalf + sw128(lt, c & 7), src + 8 * c);
+        }
+        cp_async_arrive(&sh->q_full[bb]);
+        ++tile;
+        return true;
+      };
+      // the unit's first two query tiles go out before the wait for K and V^T (the previous
+      // unit's products), so the first product of the unit waits only on the dequantisation
+      int j = 0;
+      for (; j < nt && j < 2 && !failed; ++j) failed = !gather(j);
+      if (failed) break;
       if (!mbar_wait_warp(&sh->raw_full, nunit & 1) || (nunit > 0 && !mbar_wait_warp(&sh->kv_free, (nunit - 1) & 1))) {
         failed = true;
         break;
@@ -357,33 +379,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
       const int64_t un = tc_next_unit(w, u + gridDim.x, units, MB, f0, f1);
       if (un < units && lt == 0) issue_page(un);
       pending = un < units;
-      const int32_t* ent = w.ent + static_cast<int64_t>(bg) * E;
-      // thread lt gathers row lt of every tile: (token slot lt / Hg, head lt % Hg)
-      const int tl = lt / Hg, hh = lt % Hg;
-      const bool has_row = tl < tok_per_tile;  // (with 128 % Hg != 0 the last rows are unused)
-      int et_next = (has_row && e0 + tl < e1) ? ent[e0 + tl] : -1;
-      for (int e = e0; e < e1 && !failed; e += tok_per_tile, ++tile) {
-        const int bb = tile & 1;
-        const int et = et_next;
-        et_next = (has_row && e + tok_per_tile + tl < e1) ? ent[e + tok_per_tile + tl] : -1;  // a tile early
-        if (tile >= 2 && !mbar_wait(&sh->q_empty[bb], ((tile >> 1) - 1) & 1)) {
-          failed = true;
-          break;
-        }
-        int2 m = make_int2(-1, -1);
-        if (et >= 0 && lt < kBmRows) {
-          const int t = et >> 4, s = et & 15;
-          const int64_t qrow = (static_cast<int64_t>(b) * T + t) * H + g * Hg + hh;
-          const __half* src = w.q16 + qrow * kDim;
-          const uint32_t q = smem_u32(qt + bb * kTcTile);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) cp_async16(q + (c >> 3) * kTcHalf + sw128(lt, c & 7), src + 8 * c);
-          m.x = static_cast<int>(qrow * kTopK + s);
-          m.y = (L - T + t) - n * kBlock;
-        }
-        sh->meta[tile & 3][lt] = m;
-        cp_async_arrive(&sh->q_full[bb]);
-      }
+      for (; j < nt && !failed; ++j) failed = !gather(j);
       u = un;
       e0 = f0;
       e1 = f1;
@@ -468,29 +464,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int tile = 0;
     int e0, e1;
+    // the row of each tile: (token slot row / Hg, head row % Hg) of the unit's entries
+    const int tl = row / Hg, hh = row % Hg;
+    const bool has_row = tl < tok_per_tile;
     for (int64_t u = tc_next_unit(w, blockIdx.x, units, MB, e0, e1); u < units && !failed;
          u = tc_next_unit(w, u + gridDim.x, units, MB, e0, e1)) {
+      const int bg = static_cast<int>(u / MB), n = static_cast<int>(u % MB), b = bg / G, g = bg % G;
+      const int L = a.seq_lens[b];
+      const int32_t* ent = w.ent + static_cast<int64_t>(bg) * E;
       for (int e = e0; e < e1 && !failed; e += tok_per_tile, ++tile) {
         if ((tile & 1) != wg) continue;
         const int bb = wg, k = tile >> 1;
+        // the row's partial-state index (-1: no row) and last visible key, read from the CSR
+        // while the product is in flight
+        const int et = (has_row && e + tl < e1) ? ent[e + tl] : -1;
+        int2 m = make_int2(-1, -1);
+        if (et >= 0) {
+          const int t = et >> 4;
+          m.x = static_cast<int>(((static_cast<int64_t>(b) * T + t) * H + g * Hg + hh) * kTopK + (et & 15));
+          m.y = (L - T + t) - n * kBlock;
+          if (m.x >= slots) m.x = -1;  // defensive: every valid entry indexes below slots
+        }
         if (!mbar_wait_warp(&sh->s_full[bb], k & 1)) {
           failed = true;
           break;
         }
         tc_fence_after();
-        int2 m = sh->meta[tile & 3][row];
-        if (m.x >= slots) m.x = -1;  // defensive: every index the loaders write is below slots
         const int lim = m.y;
-        // pass 1: the row maximum over the visible keys
+        // pass 1: the row maximum over the visible keys (64-column loads: each TMEM round trip
+        // is a full wait, so fewer and wider loads)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c0 = 0; c0 < kBlock; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(trow + bb * 128 + c0, v);
+        for (int c0 = 0; c0 < kBlock; c0 += 64) {
+          uint32_t v[64];
+          tmem_ld64(trow + bb * 128 + c0, v);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (c0 + 63 <= lim) {  // the whole chunk is visible (every chunk but the causal edge)
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            mx4[j & 3] = fmaxf(mx4[j & 3], c0 + j <= lim ? __uint_as_float(v[j]) : -INFINITY);
+            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(v[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              mx4[j & 3] = fmaxf(mx4[j & 3], c0 + j <= lim ? __uint_as_float(v[j]) : -INFINITY);
+          }
         }
         const float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float mscaled = lim >= 0 ? mrow * a.scale_log2 : 0.f;
@@ -502,24 +518,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
         uint8_t* prow = pt + bb * kTcTile;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c0 = 0; c0 < kBlock; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(trow + bb * 128 + c0, v);
+        for (int c0 = 0; c0 < kBlock; c0 += 64) {
+          uint32_t v[64];
+          tmem_ld64(trow + bb * 128 + c0, v);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          uint32_t pk[16];
+          if (c0 + 63 <= lim) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float p0 = c0 + j <= lim ? bm_exp2(fmaf(__uint_as_float(v[j]), a.scale_log2, -mscaled)) : 0.f;
-            const float p1 = c0 + j + 1 <= lim ? bm_exp2(fmaf(__uint_as_float(v[j + 1]), a.scale_log2, -mscaled)) : 0.f;
-            l4[(j >> 1) & 3] += p0 + p1;
-            pk[j >> 1] = pack_f16x2(p0, p1);
+            for (int j = 0; j < 64; j += 2) {
+              const float p0 = bm_exp2(fmaf(__uint_as_float(v[j]), a.scale_log2, -mscaled));
+              const float p1 = bm_exp2(fmaf(__uint_as_float(v[j + 1]), a.scale_log2, -mscaled));
+              l4[(j >> 1) & 3] += p0 + p1;
+              v[j >> 1] = pack_f16x2(p0, p1);  // packed in place: pair j / 2
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+              const float p0 = c0 + j <= lim ? bm_exp2(fmaf(__uint_as_float(v[j]), a.scale_log2, -mscaled)) : 0.f;
+              const float p1 =
+                  c0 + j + 1 <= lim ? bm_exp2(fmaf(__uint_as_float(v[j + 1]), a.scale_log2, -mscaled)) : 0.f;
+              l4[(j >> 1) & 3] += p0 + p1;
+              v[j >> 1] = pack_f16x2(p0, p1);
+            }
           }
-          uint8_t* hdst = prow + (c0 >= 64 ? kTcHalf : 0);
-          const int ch = (c0 & 63) >> 3;
+          uint8_t* hdst = prow + (c0 >= 64 ? kTcHalf : 0);  // keys 64h .. 64h+63: SW128 half h
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(hdst + sw128(row, ch + q)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(hdst + sw128(row, q)) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
         const float lrow = (l4[0] + l4[1]) + (l4[2] + l4[3]);
         fence_proxy_async_smem();
@@ -529,30 +553,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
           mbar_arrive(&sh->s_empty[bb]);
           mbar_arrive(&sh->p_full[bb]);
         }
-        // epilogue: O row / l as f16 into the row's partial slot, with (m, l)
+        // epilogue: O row / l as f16, staged in the P buffer (its product is done) at exactly the
+        // bytes the P layout gives the same row -- dims 64h .. 64h+63 in half h, 128-byte swizzle
+        // -- so that a warp touches only its own rows while the warpgroup's faster warps already
+        // write the next tile's P; then one coalesced 256-byte store per row into the row's
+        // partial slot, with (m, l)
         if (!mbar_wait_warp(&sh->o_full[bb], k & 1)) {
           failed = true;
           break;
         }
         tc_fence_after();
         const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-        __half* dst = m.x >= 0 ? w.po + static_cast<int64_t>(m.x) * kDim : nullptr;
+        uint8_t* stage = pt + bb * kTcTile;
 #pragma unroll
-        for (int c0 = 0; c0 < kDim; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(trow + 256 + bb * 128 + c0, v);
+        for (int c0 = 0; c0 < kDim; c0 += 64) {
+          uint32_t v[64];
+          tmem_ld64(trow + 256 + bb * 128 + c0, v);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (dst != nullptr) {
-            uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2)
-              pk[j >> 1] = pack_f16x2(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+          for (int j = 0; j < 64; j += 2) v[j >> 1] = pack_f16x2(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(dst + c0 + 8 * q) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(stage + (c0 >> 6) * kTcHalf + sw128(row, q)) =
+                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
-        if (dst != nullptr) w.pm[m.x] = make_float2(mscaled, lrow);
+        __syncwarp();
+#pragma unroll 1
+        for (int r8 = 0; r8 < 32; r8 += 8) {  // 8 rows at a time: independent loads, then stores
+          int px[8];
+          uint2 val[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r2 = quarter * 32 + r8 + i;
+            px[i] = __shfl_sync(0xffffffffu, m.x, r8 + i);
+            val[i] = *reinterpret_cast<const uint2*>(stage + (lane >> 4) * kTcHalf + sw128(r2, (lane & 15) >> 1) +
+                                                     8 * (lane & 1));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (px[i] >= 0) *reinterpret_cast<uint2*>(w.po + static_cast<int64_t>(px[i]) * kDim + 4 * lane) = val[i];
+        }
+        __syncwarp();
+        if (m.x >= 0) w.pm[m.x] = make_float2(mscaled, lrow);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->o_empty[bb]);
