@@ -144,10 +144,10 @@ __global__ void __launch_bounds__(kBmThreads) bm_scatter_kernel(const AttnArgs a
 
 // ---- tcgen05 block attention ------------------------------------------------------------
 // Warp roles of bm_attn_kernel: warps 0-7 softmax + epilogue (warpgroup w = warp / 4 owns the
-// tiles of parity w and their buffers; TMEM lane quarter warp % 4), warps 8-11 loaders (the
-// unit's page copy and its dequantisation, the query tiles), warp 12 the MMA issuer.
+// tiles of parity w and their buffers; TMEM lane quarter warp % 4), warps 8-10 loaders (the
+// unit's page copy and its dequantisation, the query tiles), warp 11 the MMA issuer.
 constexpr int kTcSmWarps = 8;
-constexpr int kTcLdWarps = 4;
+constexpr int kTcLdWarps = 3;  // (12 warps in all: 168 registers a thread, no spills)
 constexpr int kTcMmaWarp = kTcSmWarps + kTcLdWarps;
 constexpr int kTcThreads = (kTcMmaWarp + 1) * 32;
 constexpr int kTcHalf = kBmRows * 128;  // [128 rows x 64 f16] K-major SW128 half tile: 16 KB
@@ -177,9 +177,8 @@ __device__ __forceinline__ int64_t tc_next_unit(const BmWorkspace& w, int64_t u,
 // K tile from the raw page: rows = keys, K = dims (the prefill indexer's octet mapping: an
 // octet's 16-byte loads and swizzled stores hit 8 distinct bank groups)
 __device__ __forceinline__ void tc_dequant_k(const uint8_t* src, uint8_t* kdst, int lt) {
-#pragma unroll
-  for (int u = 0; u < kBlock * 4 / (kTcLdWarps * 32); ++u) {
-    const int item = lt + u * kTcLdWarps * 32;
+#pragma unroll 2
+  for (int item = lt; item < kBlock * 4; item += kTcLdWarps * 32) {
     const int i8 = item & 7, oct = item >> 3;
     const int r = 4 * (oct >> 1) + (i8 & 1) + 2 * (((i8 >> 1) & 1) ^ (oct & 1));
     const int c = i8 >> 1;  // dims 32c .. 32c+31
@@ -212,8 +211,7 @@ __device__ __forceinline__ void tc_dequant_k(const uint8_t* src, uint8_t* kdst, 
 // by byte permutes into one 16-byte chunk (8 keys) of each of the 8 dim rows.
 __device__ __forceinline__ void tc_dequant_vt(const uint8_t* src, uint8_t* vdst, int lt) {
 #pragma unroll 1
-  for (int u = 0; u < (kDim / 8) * (kBlock / 8) / (kTcLdWarps * 32); ++u) {
-    const int item = lt + u * kTcLdWarps * 32;
+  for (int item = lt; item < (kDim / 8) * (kBlock / 8); item += kTcLdWarps * 32) {
     const int o = item & 15, kg = item >> 4;  // dim octet, key group
     uint32_t x[8][4];
 #pragma unroll
@@ -336,9 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
     if (u < units && lt == 0) issue_page(u);
     int nunit = 0, tile = 0;
     bool pending = u < units;  // a page copy is in flight
-    // thread lt gathers row lt of every tile: (token slot lt / Hg, head lt % Hg)
-    const int tl = lt / Hg, hh = lt % Hg;
-    const bool has_row = tl < tok_per_tile;  // (with 128 % Hg != 0 the last rows are unused)
+    // thread lt gathers rows lt, lt + 96, ... of every tile: (token slot r / Hg, head r % Hg)
     for (; u < units && !failed; ++nunit) {
       const int bg = static_cast<int>(u / MB), b = bg / G, g = bg % G;
       const int32_t* ent = w.ent + static_cast<int64_t>(bg) * E;
@@ -346,14 +342,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
       // query tile j of the unit (global tile `tile`) with its row metadata
       auto gather = [&](int j) -> bool {
         const int bb = tile & 1, e = e0 + j * tok_per_tile;
-        const int et = (has_row && e + tl < e1) ? ent[e + tl] : -1;
         if (tile >= 2 && !mbar_wait(&sh->q_empty[bb], ((tile >> 1) - 1) & 1)) return false;
-        if (et >= 0) {
-          const int64_t qrow = (static_cast<int64_t>(b) * T + (et >> 4)) * H + g * Hg + hh;
-          const __half* src = w.q16 + qrow * kDim;
-          const uint32_t q = smem_u32(qt + bb * kTcTile);
+        const uint32_t q = smem_u32(qt + bb * kTcTile);
+        for (int r = lt; r < kBmRows; r += kTcLdWarps * 32) {
+          const int tl = r / Hg;  // (with 128 % Hg != 0 the last rows are unused)
+          const int et = (tl < tok_per_tile && e + tl < e1) ? ent[e + tl] : -1;
+          if (et >= 0) {
+            const int64_t qrow = (static_cast<int64_t>(b) * T + (et >> 4)) * H + g * Hg + r % Hg;
+            const __half* src = w.q16 + qrow * kDim;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) cp_async16(q + (c >> 3) * kTcHalf + sw128(lt, c & 7), src + 8 * c);
+            for (int c = 0; c < 16; ++c) cp_async16(q + (c >> 3) * kTcHalf + sw128(r, c & 7), src + 8 * c);
+          }
         }
         cp_async_arrive(&sh->q_full[bb]);
         ++tile;
@@ -491,25 +490,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
         }
         tc_fence_after();
         const int lim = m.y;
-        // pass 1: the row maximum over the visible keys (64-column loads: each TMEM round trip
-        // is a full wait, so fewer and wider loads)
+        // the row of S in registers: two 64-column loads, one wait (each TMEM wait is a full
+        // round trip); pass 1 the maximum over the visible keys, pass 2 the exponentials
+        uint32_t sv[2][64];
+        tmem_ld64(trow + bb * 128, sv[0]);
+        tmem_ld64(trow + bb * 128 + 64, sv[1]);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c0 = 0; c0 < kBlock; c0 += 64) {
-          uint32_t v[64];
-          tmem_ld64(trow + bb * 128 + c0, v);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (c0 + 63 <= lim) {  // the whole chunk is visible (every chunk but the causal edge)
+        for (int h = 0; h < 2; ++h) {
+          if (64 * h + 63 <= lim) {  // the whole half is visible (every half but the causal edge)
 #pragma unroll
-            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(v[j]));
+            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[h][j]));
           } else {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-              mx4[j & 3] = fmaxf(mx4[j & 3], c0 + j <= lim ? __uint_as_float(v[j]) : -INFINITY);
+              mx4[j & 3] = fmaxf(mx4[j & 3], 64 * h + j <= lim ? __uint_as_float(sv[h][j]) : -INFINITY);
           }
         }
         const float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float mscaled = lim >= 0 ? mrow * a.scale_log2 : 0.f;
+        // S is read: the next tile's product may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->s_empty[bb]);
         // pass 2: p = 2^(s c - m) (0 where masked), the row sum, P as f16 (A operand of P V)
         if (k >= 1 && !mbar_wait_warp(&sh->p_empty[bb], (k - 1) & 1)) {
           failed = true;
@@ -518,11 +522,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
         uint8_t* prow = pt + bb * kTcTile;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c0 = 0; c0 < kBlock; c0 += 64) {
-          uint32_t v[64];
-          tmem_ld64(trow + bb * 128 + c0, v);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (c0 + 63 <= lim) {
+        for (int h = 0; h < 2; ++h) {
+          uint32_t* v = sv[h];
+          if (64 * h + 63 <= lim) {
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
               const float p0 = bm_exp2(fmaf(__uint_as_float(v[j]), a.scale_log2, -mscaled));
@@ -533,26 +535,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
           } else {
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
-              const float p0 = c0 + j <= lim ? bm_exp2(fmaf(__uint_as_float(v[j]), a.scale_log2, -mscaled)) : 0.f;
+              const float p0 = 64 * h + j <= lim ? bm_exp2(fmaf(__uint_as_float(v[j]), a.scale_log2, -mscaled)) : 0.f;
               const float p1 =
-                  c0 + j + 1 <= lim ? bm_exp2(fmaf(__uint_as_float(v[j + 1]), a.scale_log2, -mscaled)) : 0.f;
+                  64 * h + j + 1 <= lim ? bm_exp2(fmaf(__uint_as_float(v[j + 1]), a.scale_log2, -mscaled)) : 0.f;
               l4[(j >> 1) & 3] += p0 + p1;
               v[j >> 1] = pack_f16x2(p0, p1);
             }
           }
-          uint8_t* hdst = prow + (c0 >= 64 ? kTcHalf : 0);  // keys 64h .. 64h+63: SW128 half h
+          uint8_t* hdst = prow + h * kTcHalf;  // keys 64h .. 64h+63: SW128 half h
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             *reinterpret_cast<uint4*>(hdst + sw128(row, q)) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
         const float lrow = (l4[0] + l4[1]) + (l4[2] + l4[3]);
         fence_proxy_async_smem();
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sh->s_empty[bb]);
-          mbar_arrive(&sh->p_full[bb]);
-        }
+        if (lane == 0) mbar_arrive(&sh->p_full[bb]);
         // epilogue: O row / l as f16, staged in the P buffer (its product is done) at exactly the
         // bytes the P layout gives the same row -- dims 64h .. 64h+63 in half h, 128-byte swizzle
         // -- so that a warp touches only its own rows while the warpgroup's faster warps already
@@ -565,17 +563,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
         tc_fence_after();
         const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
         uint8_t* stage = pt + bb * kTcTile;
-#pragma unroll
-        for (int c0 = 0; c0 < kDim; c0 += 64) {
-          uint32_t v[64];
-          tmem_ld64(trow + 256 + bb * 128 + c0, v);
+        {
+          uint32_t ov[2][64];
+          tmem_ld64(trow + 256 + bb * 128, ov[0]);
+          tmem_ld64(trow + 256 + bb * 128 + 64, ov[1]);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) v[j >> 1] = pack_f16x2(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t* v = ov[h];
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(stage + (c0 >> 6) * kTcHalf + sw128(row, q)) =
-                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int j = 0; j < 64; j += 2)
+              v[j >> 1] = pack_f16x2(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(stage + h * kTcHalf + sw128(row, q)) =
+                  make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
         }
         __syncwarp();
 #pragma unroll 1
