@@ -54,7 +54,8 @@ def measured_tensor_peak():
 KERNEL_SOURCES = {
     "indexer_half_kernel": ["indexer.cu", "msa_device.cuh", "msa_kernels.h"],
     "indexer_kernel": ["indexer.cu", "msa_device.cuh", "msa_kernels.h"],
-    "prefill_indexer_kernel": ["prefill.cu", "msa_device.cuh", "msa_kernels.h"],
+    "prefill_indexer_kernel": ["prefill.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
+    "bm_attn_kernel": ["prefill_attn.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "attention_kernel": ["attention.cu", "msa_device.cuh", "msa_kernels.h"],
 }
 
@@ -396,7 +397,15 @@ def run_ours(args):
     idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
     att_gbs = kv_bytes / (att_ms / 1e3) / 1e9
     step_gbs = (idx_bytes + kv_bytes) / (ms_step / 1e3) / 1e9
-    launches_per_step = 4  # indexer, select, attention, partial merge
+    # indexer, select, then the team attention and its partial merge, or (from 64 query tokens
+    # on) the block-major attention: CSR count, scan and scatter, f16 queries, tcgen05 block
+    # attention, log-sum-exp merge (its counter memset is not a kernel)
+    block_major = T >= 64
+    launches_per_step = 8 if block_major else 4
+    # attention FLOPs: QK and PV, 2 * 128 each, per (query head, visible selected key)
+    pos_bt = dw.lens[:, None] - T + np.arange(T)[None, :]
+    vis = np.clip(pos_bt[:, :, None, None] - 128 * sel_h.astype(np.int64) + 1, 0, 128) * (sel_h >= 0)
+    att_flops = 4.0 * 128 * (H // 4) * float(np.sum(vis))
     idx_kernel = indexer_kernel_for(T, 4)
     traffic = measured_traffic(idx_kernel, w.name)
     if idx_kernel == "prefill_indexer_kernel":
@@ -429,6 +438,8 @@ def run_ours(args):
         "roofline": roofline,
         "stages_ms": {"indexer": idx_ms, "select": sel_ms, "attention": att_ms,
                       "attention_gbs": att_gbs, "attention_bytes": kv_bytes},
+        "attention_form": "block-major (K-to-Q CSR, tcgen05)" if block_major else "query-major teams (mma.sync)",
+        "attention_tflops": att_flops / (att_ms / 1e3) / 1e12,
         "e2e": {"value": ws * queries / e2e_s, "unit": "queries/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
