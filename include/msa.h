@@ -179,18 +179,27 @@ msa_status_t msa_indexer_scores(const msa_config_t* cfg, const msa_cache_t* cach
 msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch, const float* block_scores,
                                int32_t* selection, void* stream);
 
-/* Stage 3 -- exact sparse GQA attention over the selected blocks (the selected pages of all
- * rows are split evenly across the GPU, online softmax, partial states merged).  Every head h of group g attends, with
- * logits (q . k) * softmax_scale, to the visible keys of selection[b][t][g][:];
+/* Stage 3 -- exact sparse GQA attention over the selected blocks.  Every head h of group g
+ * attends, with logits (q . k) * softmax_scale, to the visible keys of selection[b][t][g][:];
  * K/V are dequantised exactly from NVFP4 in the kernel.  out is rounded to bfloat16;
- * lse may be NULL.  workspace: msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...). */
+ * lse may be NULL.  workspace: msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...).
+ * Below 64 query tokens per sequence the selected pages of all rows are split evenly across
+ * the GPU (online softmax, split rows' partial states merged).  From 64 tokens on (chunked
+ * prefill) the attention is KV-block-major ("MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0
+ * 部署", the query-major versus KV-block-major scheduling of the sparse GQA step): the
+ * selections are inverted into a per-block list of (token, slot) entries, each selected
+ * block is loaded once for all the tokens that chose it, and every (token, head) merges its
+ * per-block partial states by log-sum-exp; its workspace then holds B*T*H*16 partial states
+ * of 264 bytes (o / l in fp16, m and l in fp32) and the queries in fp16.  Both forms give
+ * the same attention within the stated tolerances, and each is bit-reproducible. */
 msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                                     const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Fused decode step = stage 1 + stage 2 + stage 3 on one stream, intermediate scores and
  * selections kept in the workspace.  selection_out (may be NULL) receives a copy of the
- * selection.  workspace: msa_workspace_bytes(MSA_OP_DECODE, ...). */
+ * selection.  workspace: msa_workspace_bytes(MSA_OP_DECODE, ...) (the stage-3 form follows
+ * the same 64-token rule as msa_sparse_attn_decode). */
 msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                         const uint8_t* q, const uint8_t* index_q, uint16_t* out, float* lse,
                         int32_t* selection_out, void* workspace, size_t workspace_bytes, void* stream);
@@ -204,9 +213,9 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
  * (partial softmax states of rows shared by two CTAs, and the device error word) lives in
  * one library-owned device array of 8 MiB, which every GPU that loads the library holds
  * until the process exits.  Nothing is allocated or freed.
- *   - A call whose msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...) exceeds 8 MiB is rejected
- *     with MSA_ERR_WORKSPACE before anything is launched.  (This build's attention needs
- *     4.0 MB whatever the batch, so every valid call fits.)
+ *   - It always runs the query-major form (whatever the number of query tokens), whose
+ *     scratch is 4.0 MB whatever the batch, so every valid call fits; a call whose scratch
+ *     would exceed 8 MiB would be rejected with MSA_ERR_WORKSPACE before any launch.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *     with that device current); make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents: calls that can
