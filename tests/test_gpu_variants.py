@@ -106,13 +106,18 @@ def test_select_variants_on_long_rows_and_ties():
             assert np.array_equal(got[:, 0, g], want), (k, init, local)
 
 
-def test_decode_variant_end_to_end():
-    """msa_decode with top_k 8, init_blocks 2, local_blocks 2 and log-sum-exp pooling."""
+@pytest.mark.parametrize("case", [("v_e2e", 2, [3000, 9000, 700]), ("v_e2e_chunk", 80, [2000, 9000])],
+                         ids=["decode_t2", "chunk_t80"])
+def test_decode_variant_end_to_end(case):
+    """msa_decode with top_k 8, init_blocks 2, local_blocks 2 and log-sum-exp pooling: two
+    query tokens (streaming indexer, team attention), and 80 (the tcgen05 prefill indexer and
+    the block-major attention, half of whose selection slots are then empty)."""
     need_gpu()
     import torch
     import block_sparse_attention_indexer_gb300 as msa
     k, init, local = 8, 2, 2
-    w, lens = syn.custom("v_e2e", 303, 3, 2, 4, [3000, 9000, 700], shuffled=True)
+    name, q_len, ctx = case
+    w, lens = syn.custom(name, 303, len(ctx), q_len, 4, ctx, shuffled=True)
     dw = device_workload(w, lens)
     cfg = dataclasses.replace(dw.cfg, top_k=k, init_blocks=init, local_blocks=local, score_type=msa.MSA_SCORE_LSE)
     B, T, H = w.batch, w.q_len, w.num_heads
@@ -141,7 +146,7 @@ def test_decode_variant_end_to_end():
                     thr = min(ref_s[b, t, g, n] for n in e - forced)
                     for n in a ^ e:
                         assert abs(ref_s[b, t, g, n] - thr) <= NEAR_TIE_REL * abs(thr), (b, t, g, n)
-    assert same.sum() >= same.size - 1
+    assert same.sum() >= same.size - max(1, same.size // 50)
     out_ref, lse_ref = OM.sparse_attention(q, *cache[:4], table, lens, ref_sel[..., :k], w.heads_per_group)
     assert_out_close(out[same], out_ref[same])
     assert np.allclose(lse[same], lse_ref[same], rtol=1e-4, atol=1e-4)
