@@ -9,6 +9,7 @@ namespace msa {
 constexpr int kSelWarps = 4;
 constexpr int kSelCap = 512;
 
+template <int KPL>
 __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs a) {
   extern __shared__ __align__(16) uint32_t sord_all[];  // [kSelWarps][row_cap] staged score orders
   __shared__ uint64_t buf[kSelWarps][kSelCap];
@@ -29,7 +30,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs
     return;
   }
   const int r = (L - a.q_len + t) / kBlock;
-  const int id = select_row_warp(a.block_scores + row * a.max_blocks, r, a.top_k, a.init_blocks, a.local_blocks, lane,
+  const int id = select_row_warp<KPL>(a.block_scores + row * a.max_blocks, r, a.top_k, a.init_blocks, a.local_blocks, lane,
                                  sord_all + static_cast<int64_t>(warp) * a.row_cap, a.row_cap, buf[warp], kSelCap);
   if (lane < kTopK) out[lane] = id;
 }
@@ -123,7 +124,12 @@ cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
   // are read from L2 on each pass
   a.row_cap = a.max_blocks < 4096 ? a.max_blocks : 4096;
   const size_t smem = static_cast<size_t>(kSelWarps) * a.row_cap * sizeof(uint32_t);
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(select_kernel), smem);
+  // rows of up to 768 candidates (e.g. chunked prefill on a 96K context) keep 24 candidates
+  // per lane in registers instead of 32: fewer registers, more rows in flight per SM
+  const bool short_rows = a.max_blocks <= 32 * 24;
+  const void* kern = short_rows ? reinterpret_cast<const void*>(select_kernel<24>)
+                                : reinterpret_cast<const void*>(select_kernel<32>);
+  cudaError_t e = ensure_dynamic_smem(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((nrows + kSelWarps - 1) / kSelWarps));
@@ -135,7 +141,7 @@ cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, select_kernel, a);
+  e = short_rows ? cudaLaunchKernelEx(&cfg, select_kernel<24>, a) : cudaLaunchKernelEx(&cfg, select_kernel<32>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -100,26 +100,29 @@ __device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v, int lane) {
 // s: the row's block scores (global); sord: optional shared staging of row_cap score orders
 // for more than 1,024 candidates (else they are re-read from L2); cb: a shared buffer of
 // cap >= 32 survivor keys.  All 32 lanes call it together.
+// KPL: candidates per lane held in registers (rows of up to 32 * KPL candidates); fewer
+// registers for short rows let more warps share an SM.
+template <int KPL = 32>
 __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, int W, int lane, uint32_t* sord,
                                                int row_cap, uint64_t* cb, int cap) {
   if (W <= 0) return -1;
   const int nc = hi - lo;                 // candidates
-  const bool in_regs = nc <= 32 * 32;     // candidate orders held in registers
+  const bool in_regs = nc <= 32 * KPL;    // candidate orders held in registers
   const bool staged = !in_regs && sord != nullptr && nc <= row_cap;
 
   // 1. score orders of the candidates, with the lane maxima; the W-th largest lane maximum
   //    bounds the winners from below (W lanes each hold a candidate at least that large)
-  uint32_t o[32];
+  uint32_t o[KPL];
   uint32_t lmax = 0;
   if (in_regs) {
-    float v[32];
+    float v[KPL];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < KPL; ++k) {
       const int c = 32 * k + lane;
       v[k] = c < nc ? __ldcg(s + lo + c) : 0.f;
     }
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < KPL; ++k) {
       o[k] = (32 * k + lane < nc) ? score_order(v[k]) : 0u;
       lmax = max(lmax, o[k]);
     }
@@ -154,7 +157,7 @@ __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, i
   int cnt = 0;
   if (in_regs) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) cnt += (32 * k + lane < nc && o[k] >= bound) ? 1 : 0;
+    for (int k = 0; k < KPL; ++k) cnt += (32 * k + lane < nc && o[k] >= bound) ? 1 : 0;
   } else {
     for (int c = lane; c < nc; c += 32) cnt += order_of(c) >= bound ? 1 : 0;
   }
@@ -169,7 +172,7 @@ __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, i
     int idx = incl - cnt;
     if (in_regs) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      for (int k = 0; k < KPL; ++k) {
         const int c = 32 * k + lane;
         if (c < nc && o[k] >= bound) cb[idx++] = key_of(o[k], lo + c);
       }
@@ -220,7 +223,7 @@ __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, i
         }
       } else if (in_regs) {  // the survivors overflowed the buffer: scan the whole row
 #pragma unroll
-        for (int kk = 0; kk < 32; ++kk) {
+        for (int kk = 0; kk < KPL; ++kk) {
           const int c = 32 * kk + lane;
           const uint64_t k = c < nc ? key_of(o[kk], lo + c) : 0ull;
           if (k < prev && k > best) best = k;
@@ -247,13 +250,14 @@ __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, i
 // local_blocks <= top_k <= 16; with r + 1 <= top_k every block 0 .. r).  Lane i < 16 gets
 // the i-th id (-1 past the end).  The recipe (top_k 16, init 0, local 1) is r plus the 15
 // best blocks before it.
+template <int KPL = 32>
 __device__ __forceinline__ int select_row_warp(const float* s, int r, int top_k, int init_blocks, int local_blocks,
                                                int lane, uint32_t* sord, int row_cap, uint64_t* cb, int cap) {
   if (r + 1 <= top_k) return (lane < kTopK && lane <= r) ? lane : -1;
   // here r >= top_k, so the init blocks, the candidates and the local window are disjoint
   // and in that order: [0, I) [I, r - Lc + 1) [r - Lc + 1, r]
   const int W = top_k - init_blocks - local_blocks;
-  const int win = top_blocks_warp(s, init_blocks, r - local_blocks + 1, W, lane, sord, row_cap, cb, cap);
+  const int win = top_blocks_warp<KPL>(s, init_blocks, r - local_blocks + 1, W, lane, sord, row_cap, cb, cap);
   const int from_win = __shfl_sync(0xffffffffu, win, (lane - init_blocks) & 31);
   if (lane < init_blocks) return lane;
   if (lane < init_blocks + W) return from_win;
