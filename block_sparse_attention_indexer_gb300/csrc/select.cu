@@ -8,6 +8,7 @@ namespace msa {
 
 constexpr int kSelWarps = 4;
 constexpr int kSelCap = 512;
+constexpr int64_t kSplitMaxRows = 2048;  // rows up to which a CTA per row beats a warp per row
 
 template <int KPL>
 __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs a) {
@@ -35,15 +36,19 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs
   if (lane < kTopK) out[lane] = id;
 }
 
-// Rows longer than 1,024 candidates (long contexts): one CTA per row.  Each of its eight
-// warps takes the best of a contiguous eighth of the candidates (the row's winners are
-// among the union of the eighths' winners), and the first warp picks the winners among
-// those at most 8 x 16 by rounds of warp arg-max over their exact keys.
-constexpr int kLongWarps = 8;
-
-__global__ void __launch_bounds__(kLongWarps * 32) select_long_kernel(const SelectArgs a) {
-  __shared__ uint64_t buf[kLongWarps][kSelCap / 8];
-  __shared__ int32_t part[kLongWarps][kTopK];
+// One CTA per row, for rows longer than 1,024 candidates (long contexts: 8 warps) and for
+// batches with few rows (decode: 4 warps, so that the row's loads and ranking are split
+// four ways instead of waiting on one warp).  Each warp takes the best of a contiguous
+// share of the candidates (the row's winners are among the union of the shares' winners,
+// at most NW x 16 keys); the first warp ranks those exact keys against each other -- each
+// lane holds NW / 2 of them and compares them with every key by shuffles -- and each of the
+// W winners writes its block id at its rank, then a warp sort puts them in ascending order.
+template <int NW, int KPL>
+__global__ void __launch_bounds__(NW * 32) select_split_kernel(const SelectArgs a) {
+  constexpr int kKeys = NW * kTopK / 32;  // candidate keys per lane in the final ranking
+  __shared__ uint64_t buf[NW][kSelCap / 8];
+  __shared__ int32_t part[NW][kTopK];
+  __shared__ int32_t win_ids[kTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();
   grid_dependents_launch();
@@ -63,34 +68,39 @@ __global__ void __launch_bounds__(kLongWarps * 32) select_long_kernel(const Sele
   }
   const float* sc = a.block_scores + row * a.max_blocks;
   const int lo = a.init_blocks, hi = r - a.local_blocks + 1, W = a.top_k - a.init_blocks - a.local_blocks;
-  const int span = (hi - lo + kLongWarps - 1) / kLongWarps;
+  const int span = (hi - lo + NW - 1) / NW;
   const int wlo = min(hi, lo + warp * span), whi = min(hi, wlo + span);
   const int ww = min(W, whi - wlo);
-  const int id = top_blocks_warp(sc, wlo, whi, ww, lane, nullptr, 0, buf[warp], kSelCap / 8);
+  const int id = top_blocks_warp<KPL>(sc, wlo, whi, ww, lane, nullptr, 0, buf[warp], kSelCap / 8);
   if (lane < kTopK) part[warp][lane] = id;
   __syncthreads();
   if (warp != 0) return;
-  // winners among the warps' winners: W rounds of warp arg-max over exact keys
-  uint64_t key[kLongWarps * kTopK / 32];
+  // exact keys of the shares' winners (0: empty slot, below every key)
+  uint64_t key[kKeys];
 #pragma unroll
-  for (int i = 0; i < kLongWarps * kTopK / 32; ++i) {
+  for (int i = 0; i < kKeys; ++i) {
     const int n = (&part[0][0])[32 * i + lane];
     key[i] = n >= 0 ? (static_cast<uint64_t>(score_order(__ldcg(sc + n))) << 32) |
                           static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(n))
                     : 0ull;
   }
-  int mine = 0x7fffffff;
-  uint64_t prev = ~0ull;
-  for (int round = 0; round < W; ++round) {
-    uint64_t best = 0;
+  // rank of each key = keys larger than it (all keys distinct)
+  int rank[kKeys];
 #pragma unroll
-    for (int i = 0; i < kLongWarps * kTopK / 32; ++i)
-      if (key[i] < prev && key[i] > best) best = key[i];
-    best = warp_max_u64(best);
-    prev = best;
-    if (lane == round) mine = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best));
-  }
-  const int sorted_id = warp_sort_asc_i32(mine, lane);
+  for (int i = 0; i < kKeys; ++i) rank[i] = 0;
+#pragma unroll
+  for (int i2 = 0; i2 < kKeys; ++i2)
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j) {
+      const uint64_t other = shfl_u64(key[i2], j);
+#pragma unroll
+      for (int i = 0; i < kKeys; ++i) rank[i] += other > key[i] ? 1 : 0;
+    }
+#pragma unroll
+  for (int i = 0; i < kKeys; ++i)
+    if (key[i] != 0ull && rank[i] < W) win_ids[rank[i]] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key[i]));
+  __syncwarp();
+  const int sorted_id = warp_sort_asc_i32(lane < W ? win_ids[lane] : 0x7fffffff, lane);
   const int from_win = __shfl_sync(0xffffffffu, sorted_id, (lane - a.init_blocks) & 31);
   int v = -1;
   if (lane < a.init_blocks)
@@ -106,17 +116,22 @@ cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
   SelectArgs a = a0;
   const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
   if (nrows == 0) return cudaSuccess;
-  if (a.max_blocks > 32 * 32) {  // long rows: a CTA per row
+  // long rows, or few rows (decode): a CTA per row; many rows (chunked prefill): a warp per row
+  const bool long_rows = a.max_blocks > 32 * 32;
+  if (long_rows || nrows <= kSplitMaxRows) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(nrows));
-    cfg.blockDim = dim3(kLongWarps * 32);
+    cfg.blockDim = dim3((long_rows ? 8 : 4) * 32);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, select_long_kernel, a);
+    // shares of at most 4096 / 8 = 512 (8 warps x 16 per lane) or 1024 / 4 = 256 (4 x 8)
+    // candidates stay in registers; longer rows read their shares from L2
+    cudaError_t e = long_rows ? cudaLaunchKernelEx(&cfg, select_split_kernel<8, 16>, a)
+                              : cudaLaunchKernelEx(&cfg, select_split_kernel<4, 8>, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }

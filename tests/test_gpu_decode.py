@@ -107,13 +107,17 @@ def test_deterministic_reruns():
         assert np.array_equal(x, y, equal_nan=True)
 
 
-def test_padding_rows_and_bad_inputs_flag_errors():
+@pytest.mark.parametrize("T", [2, 80], ids=["t2", "t80_block_major"])
+def test_padding_rows_and_bad_inputs_flag_errors(T):
+    """Padding rows, a length below q_len and a bad page: flagged, defined outputs, no fault --
+    for two query tokens and for 80 (the tcgen05 prefill indexer and the block-major plan,
+    which must skip the bad page's entries)."""
     need_gpu()
     import torch
     import block_sparse_attention_indexer_gb300 as msa
-    w, lens = syn.custom("bad", 12, 4, 2, 8, [3000, 3000, 3000, 3000], shuffled=False)
+    w, lens = syn.custom("bad", 12, 4, T, 8, [3000, 3000, 3000, 3000], shuffled=False)
     dw = device_workload(w, lens)
-    B, T, H = 4, 2, 32
+    B, H = 4, 32
     # sequence 1 is a padding row, sequence 2 is shorter than q_len, sequence 3 has a bad page
     seq = dw.batch.seq_lens.clone()
     seq[1] = 0
