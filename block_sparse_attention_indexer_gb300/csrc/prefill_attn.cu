@@ -155,7 +155,7 @@ constexpr int kTcTile = 2 * kTcHalf;    // 32 KB
 constexpr uint32_t kTcTmemCols = 512;   // S[2] at 0 / 128, O[2] at 256 / 384
 
 struct TcShared {
-  uint64_t raw_full, kv_full, kv_free;
+  uint64_t raw_full, kv_full, kv_free, raw_free;
   uint64_t q_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
   uint32_t tmem_base;
 };
@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
     mbar_init(&sh->raw_full, 1);
     mbar_init(&sh->kv_full, kTcLdWarps);
     mbar_init(&sh->kv_free, 1);
+    mbar_init(&sh->raw_free, kTcLdWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->q_full[b], kTcLdWarps * 32);
       mbar_init(&sh->q_empty[b], 1);
@@ -372,12 +373,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
       tc_dequant_vt(raw + kPageData + kPageScale, vt, lt);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->kv_full);
-      asm volatile("bar.sync 1, %0;" ::"r"(kTcLdWarps * 32) : "memory");  // every loader is done with raw
+      if (lane == 0) {
+        mbar_arrive(&sh->kv_full);
+        mbar_arrive(&sh->raw_free);
+      }
       int f0, f1;
       const int64_t un = tc_next_unit(w, u + gridDim.x, units, MB, f0, f1);
-      if (un < units && lt == 0) issue_page(un);
-      pending = un < units;
+      // the next page goes into the raw area once every loader is done with it (a bounded
+      // mbarrier wait, not a named barrier: a loader that gave up must not stall the rest)
+      if (un < units && lt == 0) {
+        if (mbar_wait(&sh->raw_free, nunit & 1))
+          issue_page(un);
+        else
+          failed = true;
+      }
+      if (__any_sync(0xffffffffu, failed)) failed = true;
+      pending = un < units && !failed;
+      if (failed) break;
       for (; j < nt && !failed; ++j) failed = !gather(j);
       u = un;
       e0 = f0;
