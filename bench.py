@@ -53,7 +53,7 @@ def measured_tensor_peak():
 
 KERNEL_SOURCES = {
     "indexer_half_kernel": ["indexer.cu", "msa_device.cuh", "msa_kernels.h"],
-    "indexer_kernel": ["indexer.cu", "msa_device.cuh", "msa_kernels.h"],
+    "spec_indexer_kernel": ["spec_indexer.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "prefill_indexer_kernel": ["prefill.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "bm_attn_kernel": ["prefill_attn.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "attention_kernel": ["attention.cu", "msa_device.cuh", "msa_kernels.h"],
@@ -65,7 +65,7 @@ def indexer_kernel_for(q_len: int, groups: int) -> str:
     rows = q_len * groups
     if rows <= 8:
         return "indexer_half_kernel"
-    return "indexer_kernel" if rows < 64 else "prefill_indexer_kernel"
+    return "spec_indexer_kernel" if rows < 64 else "prefill_indexer_kernel"
 
 
 def kernel_source_hash(kernel: str) -> str:

@@ -98,7 +98,9 @@ msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA
 
 // stage 1: the streaming decode indexer, or its tcgen05 GEMM form for long query chunks
 cudaError_t run_indexer(const IndexerArgs& a, int sms, cudaStream_t s) {
-  if (a.q_len * a.groups >= kPrefillMinRows) return launch_prefill_indexer(a, s);
+  const int rows = a.q_len * a.groups;
+  if (rows >= kPrefillMinRows) return launch_prefill_indexer(a, s);
+  if (rows > 8) return launch_spec_indexer(a, sms, s);
   return launch_indexer(a, sms, s);
 }
 
@@ -114,8 +116,6 @@ IndexerArgs indexer_args(const msa_config_t* cfg, const msa_cache_t* cache, cons
   a.max_blocks = batch->max_blocks;
   a.q_len = batch->q_len;
   a.groups = cfg->num_kv_groups;
-  const int tc = 32 / cfg->num_kv_groups;
-  a.chunk_tokens = batch->q_len < tc ? batch->q_len : tc;
   a.index_q = index_q;
   a.block_scores = scores;
   a.err = err;

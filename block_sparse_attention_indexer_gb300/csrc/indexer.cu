@@ -1,42 +1,39 @@
-// Stage 1 of MSA decode: indexer score + block max-pool.
+// Stage 1 of MSA decode for at most 8 query rows per sequence (T x G <= 8): indexer
+// score + block pooling.
 //
-// "Ein leichtgewichtiger Indexer bewertet jeden Schlüssel im Kontext mit einer
-// Index-Abfrage pro GQA-Gruppe gegen einen einzigen gemeinsamen Index-Schlüssel-Kopf und
-// poolt diese Bewertungen dann per Max-Pooling zu einer Bewertung pro Block" -- restated:
-// every cached key j is scored against one index query per (query token, KV group), and
-// the scores of a 128-token block are reduced with max over the keys visible to the query
-// ("vLLM liefert Day-0-Unterstützung für MiniMax-M3.1-Flash", §MSA-Grundlagen; masks from
-// "MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署", §MSA 机制细节).
+// Every cached key j is scored against one index query per (query token, KV group) through
+// the single shared index-key head, and the scores of a 128-token block are reduced (max, or
+// log-sum-exp) over the keys visible to the query ("vLLM liefert Day-0-Unterstützung für
+// MiniMax-M3.1-Flash", §MSA-Grundlagen; masks from "MiniMax M3 x vLLM：百万 token 多模态推理的
+// Day-0 部署", §MSA 机制细节).  Longer query rows go to the tcgen05 kernels (spec_indexer.cu
+// for 9..63 rows, prefill.cu from 64 rows).
 //
 // Design (GB300): the path is HBM-bound (72 bytes of NVFP4 index key per token, read
 // once per step), so the kernel is a persistent streaming scan:
-//   * one CTA per SM, 8 independent warps; the flattened list of (sequence, page, query
-//     chunk) units is split into equal contiguous ranges, one per warp (balanced to one
-//     unit whatever the ragged lengths);
-//   * each warp streams its pages with a private 2-stage ring of 9 KB shared-memory
-//     buffers filled by bulk async copies (cp.async.bulk + mbarrier), so ~72 KB per SM is
-//     always in flight;
+//   * one CTA per SM, 16 independent warps; the flattened list of (sequence, page) units is
+//     split into equal contiguous ranges, one per warp (balanced to one page whatever the
+//     ragged lengths);
+//   * each warp streams its pages as half pages (64 keys: 4 KB of E2M1 + 512 B of scales)
+//     through a private 3-stage ring of shared-memory buffers filled by bulk async copies
+//     (cp.async.bulk + mbarrier), so ~216 KB per SM is always in flight;
 //   * scores run on the tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate) with keys
-//     as M (16 per tile) and query rows (token, group) as N: one packed E2M1 byte becomes
-//     one f16x2 A register (cvt.rn.f16x2.e2m1x2), the block scale multiplies it in f16
-//     (E2M1 x E4M3 products are exact in f16), and the FP8 index query widens exactly to
+//     as M (16 per tile) and the <= 8 query rows (token, group) as N: one packed E2M1 byte
+//     becomes one f16x2 A register (cvt.rn.f16x2.e2m1x2), the block scale multiplies it in
+//     f16 (E2M1 x E4M3 products are exact in f16), and the FP8 index query widens exactly to
 //     f16, so every product is exact and only the f32 accumulation rounds -- the exact-score
 //     idea of the Rubin section of the M3.1 post, instead of re-rounding keys to FP8;
 //   * the contraction order over the 128 dims is permuted so that each lane reads 16
 //     contiguous bytes per key row (the dot product is order-free; the queries use the same
 //     permutation);
-//   * the max-pool is a register max over the 8 key tiles of a page followed by a 3-step
-//     shuffle reduction; per-token scores never leave registers.
+//   * the block pool is a register reduction over the key tiles of a half page, a 3-step
+//     shuffle reduction, and a combine of the two halves; per-token scores never leave
+//     registers.
 #include <cuda_fp16.h>
 
 #include "msa_device.cuh"
 #include "msa_kernels.h"
 
 namespace msa {
-
-constexpr int kIdxWarps = 12;
-constexpr int kIdxStages = 2;
-constexpr int kStageBytes = kPageData + kPageScale;  // 9216
 
 __device__ __forceinline__ int find_seq(const int32_t* prefix, int batch, int64_t u) {
   // largest b with prefix[b] <= u (prefix is non-decreasing, prefix[batch] > u)
@@ -48,8 +45,8 @@ __device__ __forceinline__ int find_seq(const int32_t* prefix, int batch, int64_
   return lo;
 }
 
-// Walks the pages of one warp's unit range in order: unit u of sequence b covers page
-// (u - prefix[b]) / nchunks.  Monotone, so the sequence index only ever moves forward.
+// Walks the pages of one warp's unit range in order: unit u of sequence b is its page
+// u - prefix[b].  Monotone, so the sequence index only ever moves forward.
 struct PageCursor {
   int64_t u;      // first unit of the current page (within the warp's range)
   int b;          // its sequence
@@ -67,10 +64,10 @@ struct PageCursor {
   }
 };
 
-// Exclusive prefix over sequences of their work units (pages x query chunks); sequences with
+// Exclusive prefix over sequences of their work units (pages); sequences with
 // an invalid length get none (and flag MSA_DEVERR_BAD_SEQLEN once).  Block-wide scan, ends
 // with __syncthreads.  prefix has batch + 1 entries.
-__device__ __forceinline__ void build_prefix(const IndexerArgs& a, int nchunks, int32_t* prefix, int32_t* warp_tot,
+__device__ __forceinline__ void build_prefix(const IndexerArgs& a, int32_t* prefix, int32_t* warp_tot,
                                              int nwarps) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.q_len;
@@ -82,7 +79,7 @@ __device__ __forceinline__ void build_prefix(const IndexerArgs& a, int nchunks, 
     const int L = a.seq_lens[b];
     const bool ok = (L >= T) && (L <= cap);
     if (L != 0 && !ok && blockIdx.x == 0) flag_error(a.err, MSA_DEVERR_BAD_SEQLEN);
-    local += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
+    local += ok ? ((L + kBlock - 1) / kBlock) : 0;
   }
   int incl = local;
 #pragma unroll
@@ -99,7 +96,7 @@ __device__ __forceinline__ void build_prefix(const IndexerArgs& a, int nchunks, 
     prefix[b] = run;
     const int L = a.seq_lens[b];
     const bool ok = (L >= T) && (L <= cap);
-    run += ok ? ((L + kBlock - 1) / kBlock) * nchunks : 0;
+    run += ok ? ((L + kBlock - 1) / kBlock) : 0;
   }
   if (tid == blockDim.x - 1) {
     int tot = 0;
@@ -107,41 +104,6 @@ __device__ __forceinline__ void build_prefix(const IndexerArgs& a, int nchunks, 
     prefix[a.batch] = tot;
   }
   __syncthreads();
-}
-
-// Scores of one 16-key tile against NT n-tiles of 8 query rows.  Keys are the M dimension
-// (rows g and g+8 of the tile), query rows the N dimension.  Two accumulators per n-tile
-// (even / odd k-steps) halve the MMA dependency chain; the caller adds them.
-template <int NT>
-__device__ __forceinline__ void score_tile(const uint8_t* st, const uint8_t* ss, int r0, int t4,
-                                           const uint32_t (&bq)[NT][8][2], float (&acc)[NT][2][4]) {
-  const int r1 = r0 + 8;
-  const uint4 d0 = lds128(st + r0 * kRowBytes + 16 * t4);
-  const uint4 d1 = lds128(st + r1 * kRowBytes + 16 * t4);
-  const uint32_t s0 = lds16(ss + r0 * kRowScales + 2 * t4);
-  const uint32_t s1 = lds16(ss + r1 * kRowScales + 2 * t4);
-  const uint32_t sc0[2] = {e4m3_bcast_f16x2(s0, 0), e4m3_bcast_f16x2(s0, 1)};
-  const uint32_t sc1[2] = {e4m3_bcast_f16x2(s1, 0), e4m3_bcast_f16x2(s1, 1)};
-  const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
-  const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-    e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
-    e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
-    const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
-    x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
-    y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      mma_f16_16816(acc[nt][0], x0, y0, x1, y1, bq[nt][2 * w][0], bq[nt][2 * w][1]);
-      mma_f16_16816(acc[nt][1], x2, y2, x3, y3, bq[nt][2 * w + 1][0], bq[nt][2 * w + 1][1]);
-    }
-  }
 }
 
 // single-accumulator tile for one n-tile; scales converted once per row pair
@@ -170,240 +132,7 @@ __device__ __forceinline__ void score_tile1(const uint8_t* st, const uint8_t* ss
   }
 }
 
-template <int NT, bool LSE>
-__global__ void __launch_bounds__(kIdxWarps * 32, 1) indexer_kernel(const IndexerArgs a) {
-  // key tiles processed together: enough independent MMA chains per warp
-  constexpr int MG = NT == 1 ? 4 : (NT == 2 ? 2 : 1);
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kIdxWarps * kIdxStages * kStageBytes);
-  int32_t* prefix = reinterpret_cast<int32_t*>(bars + kIdxWarps * kIdxStages);
-  __shared__ int32_t warp_tot[kIdxWarps];
-
-  // launched as a programmatic dependent of the previous kernel on the stream: wait for it
-  // (and its memory) before touching global memory
-  grid_dependency_wait();
-  grid_dependents_launch();
-  const uint64_t l2_once = l2_evict_first_policy();  // every page is read once per call
-  constexpr bool lse = LSE;                             // block pooling: log-sum-exp or max
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t4 = lane & 3;
-  const int T = a.q_len, G = a.groups, TC = a.chunk_tokens;
-  const int nchunks = (T + TC - 1) / TC;
-
-  build_prefix(a, nchunks, prefix, warp_tot, kIdxWarps);
-  if (lane == 0)
-    for (int s = 0; s < kIdxStages; ++s) mbar_init(&bars[warp * kIdxStages + s], 1);
-  fence_mbar_init();
-  __syncthreads();
-
-  const int64_t total = prefix[a.batch];
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kIdxWarps;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kIdxWarps + warp;
-  const int64_t u0 = total * gw / nwarps, u1 = total * (gw + 1) / nwarps;
-
-  uint8_t* my_stages = stages + warp * kIdxStages * kStageBytes;
-  uint64_t* my_bars = bars + warp * kIdxStages;
-
-  // ---- issue side: a cursor one page ahead of the copies, whose block-table entry is
-  // loaded one issue early so that its latency hides behind a page of compute
-  PageCursor ic;
-  ic.init(prefix, a.batch, u0, u1);
-  int next_page = -1;
-  auto lookup_next = [&]() {
-    if (ic.u < u1) {
-      ic.settle(prefix);
-      const int n = static_cast<int>((ic.u - prefix[ic.b]) / nchunks);
-      next_page = __ldg(a.block_table + static_cast<int64_t>(ic.b) * a.max_blocks + n);
-    }
-  };
-  uint32_t valid_bits = 0;  // bit s: the page in stage s has a valid id
-  auto issue_next = [&](int stage) {
-    const int n = static_cast<int>((ic.u - prefix[ic.b]) / nchunks);
-    const int64_t end = prefix[ic.b] + static_cast<int64_t>(n + 1) * nchunks;
-    const int page = next_page;
-    ic.u = end < u1 ? end : u1;
-    const bool ok = page >= 0 && page < a.num_pages;
-    valid_bits = ok ? (valid_bits | (1u << stage)) : (valid_bits & ~(1u << stage));
-    if (lane == 0) {
-      uint64_t* bar = &my_bars[stage];
-      if (ok) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        uint8_t* dst = my_stages + stage * kStageBytes;
-        bulk_g2s_hint(dst, a.idx_data + static_cast<int64_t>(page) * kPageData, kPageData, bar, l2_once);
-        bulk_g2s_hint(dst + kPageData, a.idx_scale + static_cast<int64_t>(page) * kPageScale, kPageScale, bar, l2_once);
-      } else {
-        flag_error(a.err, MSA_DEVERR_BAD_PAGE);
-        mbar_arrive(bar);
-      }
-    }
-    lookup_next();
-  };
-
-  lookup_next();
-  int issued = 0;
-  for (int s = 0; s < kIdxStages && ic.u < u1; ++s, ++issued) issue_next(s);
-
-  // ---- consumer
-  uint32_t bq[NT][8][2];  // B fragments (index queries) of one chunk of one sequence
-  int cur_b = -1, cur_c = -1, L = 0;
-  PageCursor cc;
-  cc.init(prefix, a.batch, u0, u1);
-  int consumed = 0;
-  bool timed_out = false;
-
-  while (cc.u < u1) {
-    cc.settle(prefix);
-    const int b = cc.b;
-    const int64_t local = cc.u - prefix[b];
-    const int n = static_cast<int>(local / nchunks);
-    const int c_lo = static_cast<int>(local - static_cast<int64_t>(n) * nchunks);
-    const int64_t end = prefix[b] + static_cast<int64_t>(n + 1) * nchunks;
-    const int64_t uend = end < u1 ? end : u1;
-    const int c_hi = c_lo + static_cast<int>(uend - cc.u);
-    const int stage = consumed % kIdxStages;
-    const uint32_t parity = (consumed / kIdxStages) & 1;
-    const bool page_ok = (valid_bits >> stage) & 1u;
-    if (b != cur_b) L = a.seq_lens[b];
-
-    if (!mbar_wait_warp(&my_bars[stage], parity)) {
-      timed_out = true;
-      break;
-    }
-    const uint8_t* st = my_stages + stage * kStageBytes;
-
-    for (int c = c_lo; c < c_hi; ++c) {
-      const int t0 = c * TC;
-      const int tc = min(TC, T - t0);
-      const int rows = tc * G;
-      const int pos_min = L - T + t0, pos_max = pos_min + tc - 1;
-      float mx[NT][2];
-      PoolState pl[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        mx[nt][0] = mx[nt][1] = -INFINITY;
-        pl[nt][0] = pl[nt][1] = {-INFINITY, 0.f};
-      }
-
-      if (page_ok && n * kBlock <= pos_max) {
-        if (b != cur_b || c != cur_c) {
-          cur_b = b;
-          cur_c = c;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const int r = nt * 8 + g;
-            if (r < rows) {
-              const int tq = t0 + r / G, gq = r % G;
-              const uint4* src = reinterpret_cast<const uint4*>(
-                  a.index_q + ((static_cast<int64_t>(b) * T + tq) * G + gq) * kDim + 32 * t4);
-              const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
-              const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-              for (int s = 0; s < 8; ++s) {
-                bq[nt][s][0] = e4m3x2_to_f16x2(w[s]);
-                bq[nt][s][1] = e4m3x2_to_f16x2(w[s] >> 16);
-              }
-            } else {
-#pragma unroll
-              for (int s = 0; s < 8; ++s) bq[nt][s][0] = bq[nt][s][1] = 0u;
-            }
-          }
-        }
-        // per column: the query position it belongs to (for the causal / tail mask)
-        int posc[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = nt * 8 + 2 * t4 + e;
-            posc[nt][e] = col < rows ? (L - T + t0 + col / G) : -1;
-          }
-        const bool need_mask = (n + 1) * kBlock - 1 > pos_min;
-
-#pragma unroll 1
-        for (int mt0 = 0; mt0 < 8; mt0 += MG) {
-          float acc[MG][NT][2][4];
-#pragma unroll
-          for (int k = 0; k < MG; ++k) score_tile<NT>(st, st + kPageData, (mt0 + k) * 16 + g, t4, bq, acc[k]);
-#pragma unroll
-          for (int k = 0; k < MG; ++k) {
-            float v[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) v[nt][e] = acc[k][nt][0][e] + acc[k][nt][1][e];
-            if (need_mask) {
-              const int j0 = n * kBlock + (mt0 + k) * 16 + g, j1 = j0 + 8;
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (j0 > posc[nt][0]) v[nt][0] = -INFINITY;
-                if (j0 > posc[nt][1]) v[nt][1] = -INFINITY;
-                if (j1 > posc[nt][0]) v[nt][2] = -INFINITY;
-                if (j1 > posc[nt][1]) v[nt][3] = -INFINITY;
-              }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              pool_add(pl[nt][0], v[nt][0], v[nt][2], lse);
-              pool_add(pl[nt][1], v[nt][1], v[nt][3], lse);
-            }
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            pool_merge_xor(pl[nt][e], 4, lse);
-            pool_merge_xor(pl[nt][e], 8, lse);
-            pool_merge_xor(pl[nt][e], 16, lse);
-            mx[nt][e] = pool_result(pl[nt][e], lse);
-          }
-      }
-      if (g == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = nt * 8 + 2 * t4 + e;
-            if (col < rows) {
-              const int tq = t0 + col / G, gq = col % G;
-              a.block_scores[((static_cast<int64_t>(b) * T + tq) * G + gq) * a.max_blocks + n] = mx[nt][e];
-            }
-          }
-      }
-    }
-    __syncwarp();
-    ++consumed;
-    cc.u = uend;
-    if (ic.u < u1) {
-      issue_next(issued % kIdxStages);
-      ++issued;
-    }
-  }
-
-  if (timed_out) {
-    if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
-    // drain this warp's copies still in flight (bounded) before leaving
-    for (int k = consumed; k < issued; ++k) mbar_wait(&my_bars[k % kIdxStages], (k / kIdxStages) & 1);
-  }
-
-  // ---- -inf for blocks past each sequence's end (and whole rows of skipped sequences)
-  const int64_t nrows = static_cast<int64_t>(a.batch) * T * G;
-  for (int64_t row = gw; row < nrows; row += nwarps) {
-    const int b = static_cast<int>(row / (static_cast<int64_t>(T) * G));
-    const int nb = (prefix[b + 1] - prefix[b]) / nchunks;
-    float* dst = a.block_scores + row * a.max_blocks;
-    for (int n = nb + lane; n < a.max_blocks; n += 32) dst[n] = -INFINITY;
-  }
-}
-
 // ------------------------------------------------------------------------------------------
-// Variant for at most 8 query rows per sequence (T x G <= 8, one n-tile, one query chunk):
-// 16 warps per SM, each streaming half pages (64 keys: 4 KB of E2M1 + 512 B of scales)
-// through a 3-stage ring; the block max combines the two halves in registers.  Twice the
-// warps of the general kernel in the same shared memory, for more latency hiding.
 constexpr int kHWarps = 16;
 constexpr int kHStages = 3;
 constexpr int kHalfData = kPageData / 2;    // 4096
@@ -427,7 +156,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
   const int T = a.q_len, G = a.groups;
   const int rows = T * G;  // <= 8
 
-  build_prefix(a, 1, prefix, warp_tot, kHWarps);
+  build_prefix(a, prefix, warp_tot, kHWarps);
   if (lane == 0)
     for (int s = 0; s < kHStages; ++s) mbar_init(&bars[warp * kHStages + s], 1);
   fence_mbar_init();
@@ -624,41 +353,9 @@ static cudaError_t launch_half(const IndexerArgs& a, int num_sms, cudaStream_t s
   return a.lse ? launch_half_t<true>(a, num_sms, s) : launch_half_t<false>(a, num_sms, s);
 }
 
-template <int NT, bool LSE>
-static cudaError_t launch_nt_t(const IndexerArgs& a, int num_sms, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(kIdxWarps) * kIdxStages * kStageBytes +
-                      kIdxWarps * kIdxStages * sizeof(uint64_t) + (a.batch + 1) * sizeof(int32_t);
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(indexer_kernel<NT, LSE>), smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(kIdxWarps * 32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, indexer_kernel<NT, LSE>, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-template <int NT>
-static cudaError_t launch_nt(const IndexerArgs& a, int num_sms, cudaStream_t s) {
-  return a.lse ? launch_nt_t<NT, true>(a, num_sms, s) : launch_nt_t<NT, false>(a, num_sms, s);
-}
-
 cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s) {
-  const int rows = a.chunk_tokens * a.groups;
-  if (a.q_len * a.groups <= 8) return launch_half(a, num_sms, s);
-  switch ((rows + 7) / 8) {
-    case 1: return launch_nt<1>(a, num_sms, s);
-    case 2: return launch_nt<2>(a, num_sms, s);
-    case 3: return launch_nt<3>(a, num_sms, s);
-    default: return launch_nt<4>(a, num_sms, s);
-  }
+  if (a.q_len * a.groups > 8) return cudaErrorInvalidValue;  // longer rows go to the tcgen05 indexers
+  return launch_half(a, num_sms, s);
 }
 
 }  // namespace msa

@@ -15,7 +15,6 @@ struct IndexerArgs {
   const int32_t* block_table;  // [B][max_blocks]
   const int32_t* seq_lens;     // [B]
   int32_t batch, max_blocks, q_len, groups;
-  int32_t chunk_tokens;        // query tokens per work chunk (rows = chunk_tokens * groups <= 32)
   const uint8_t* index_q;      // [B][T][G][128] E4M3
   float* block_scores;         // [B][T][G][max_blocks]
   uint32_t* err;
@@ -71,6 +70,9 @@ cudaError_t launch_fp8_quantize(const float* x, int64_t n, uint8_t* out, cudaStr
 cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s);
 // tcgen05 GEMM form of the indexer for long query chunks (chunked prefill)
 cudaError_t launch_prefill_indexer(const IndexerArgs& a, cudaStream_t s);
+// tcgen05 form with the keys as M (converted in registers into tensor memory) for
+// 8 < T x G < 64 query rows per sequence (speculative decode)
+cudaError_t launch_spec_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s);
 // query rows (token x group) per sequence from which the GEMM form is used
 constexpr int kPrefillMinRows = 64;
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);

@@ -14,10 +14,11 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # name, lens, q_len, heads_per_group, shuffled
     ("ragged_t1", [1, 127, 128, 129, 1000, 4096 + 5, 2048, 16 * 128 + 1], 1, 8, True),
-    ("spec_t3", [300, 5000, 3 * 128], 3, 4, True),
-    ("spec_t8", [8, 2100, 7777], 8, 8, False),
+    ("spec_t3", [300, 5000, 3 * 128], 3, 4, True),           # 12 rows: speculative tcgen05 indexer, N 16
+    ("spec_t8", [8, 2100, 7777], 8, 8, False),               # 32 rows: N 32
+    ("spec_t15", [15, 1111, 6000 + 3], 15, 4, True),         # 60 rows: N 64, the widest speculative case
     ("chunked_t20", [640, 3000], 20, 8, True),               # 80 rows: tcgen05 GEMM indexer
-    ("chunked_t12", [1500, 999, 260], 12, 4, True),          # 48 rows: streaming indexer, 2 chunks
+    ("chunked_t12", [1500, 999, 260], 12, 4, True),          # 48 rows: speculative indexer, N 48
     ("prefill_t300", [300, 5000 + 77, 40000], 300, 8, True),  # 1,200 rows: several GEMM row tiles
     ("prefill_t96", [96, 3000 + 5], 96, 8, True),            # 384 rows: the last CTA has one full tile
     ("hg4_t1", [4096] * 3, 1, 4, False),

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # name, lens, q_len, heads_per_group, shuffled  (q_len x 4 groups picks the indexer kernel)
     ("v_ragged_t1", [1, 127, 129, 1000, 4096 + 5, 16 * 128 + 1], 1, 8, True),   # half-page kernel
-    ("v_spec_t3", [300, 5000, 3 * 128], 3, 4, True),                           # streaming kernel
+    ("v_spec_t3", [300, 5000, 3 * 128], 3, 4, True),                           # speculative tcgen05 kernel
     ("v_chunked_t20", [640, 3000], 20, 8, True),                               # tcgen05 GEMM kernel
 ]
 VARIANTS = [  # top_k, init_blocks, local_blocks
