@@ -296,24 +296,23 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_indexer_kernel(const
         if (active) {
           const uint32_t tacc = trow + static_cast<uint32_t>(acc * kPfTiles * kBlock);
           const int lim = pos - (n0 + k) * kBlock;  // columns 0 .. lim are visible to this row
-          // max: four independent chains, two 32-column loads in flight per wait
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          // max: each 64-column load also returns the maximum of what it loads (tcgen05.ld.red);
+          // only the half holding the causal limit is masked by hand (four independent chains)
 #pragma unroll
           for (int c0 = 0; c0 < kBlock; c0 += 64) {
-            uint32_t v[2][32];
-            tmem_ld32(tacc + c0, v[0]);
-            tmem_ld32(tacc + c0 + 32, v[1]);
+            uint32_t v[64];
+            float hmax;
+            tmem_ld64_max(tacc + c0, v, hmax);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             if (c0 + 63 <= lim) {
-#pragma unroll
-              for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(v[j >> 5][j & 31]));
+              mx = fmaxf(mx, hmax);
             } else {
+              float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-              for (int j = 0; j < 64; ++j)
-                m4[j & 3] = fmaxf(m4[j & 3], c0 + j <= lim ? __uint_as_float(v[j >> 5][j & 31]) : -INFINITY);
+              for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], c0 + j <= lim ? __uint_as_float(v[j]) : -INFINITY);
+              mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
             }
           }
-          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           if (lse) {
             // log-sum-exp pooling: a second pass over the accumulator, sum e^{s - max} (the
             // warp-collective loads run in every lane; a row with nothing visible stays -inf)

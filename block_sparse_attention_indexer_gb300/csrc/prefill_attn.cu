@@ -503,24 +503,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) bm_attn_kernel(const AttnArgs a
         tc_fence_after();
         const int lim = m.y;
         // the row of S in registers: two 64-column loads, one wait (each TMEM wait is a full
-        // round trip); pass 1 the maximum over the visible keys, pass 2 the exponentials
+        // round trip), each load also returning its maximum (tcgen05.ld.red); pass 1 the
+        // maximum over the visible keys, pass 2 the exponentials
         uint32_t sv[2][64];
-        tmem_ld64(trow + bb * 128, sv[0]);
-        tmem_ld64(trow + bb * 128 + 64, sv[1]);
+        float hmax[2];
+        tmem_ld64_max(trow + bb * 128, sv[0], hmax[0]);
+        tmem_ld64_max(trow + bb * 128 + 64, sv[1], hmax[1]);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mrow = -INFINITY;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (64 * h + 63 <= lim) {  // the whole half is visible (every half but the causal edge)
-#pragma unroll
-            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sv[h][j]));
+            mrow = fmaxf(mrow, hmax[h]);
           } else {
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < 64; ++j)
               mx4[j & 3] = fmaxf(mx4[j & 3], 64 * h + j <= lim ? __uint_as_float(sv[h][j]) : -INFINITY);
+            mrow = fmaxf(mrow, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
           }
         }
-        const float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float mscaled = lim >= 0 ? mrow * a.scale_log2 : 0.f;
         // S is read: the next tile's product may overwrite it
         tc_fence_before();
