@@ -38,45 +38,65 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
-// One thread per 16-element group.
-__global__ void nvfp4_insert_kernel(QuantArgs a) {
-  const int groups_per_row = a.dim / 16;
-  const int64_t groups_per_token = static_cast<int64_t>(a.rows_per_token) * groups_per_row;
-  const int64_t total = a.n_tokens * groups_per_token;
-  for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gi < total;
-       gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t tok = gi / groups_per_token;
-    const int64_t rem = gi - tok * groups_per_token;
-    const int row = static_cast<int>(rem / groups_per_row);
-    const int grp = static_cast<int>(rem - static_cast<int64_t>(row) * groups_per_row);
-    const int64_t slot = a.slots[tok];
-    if (slot < 0 || slot >= a.num_pages * a.block_size) continue;
-    const int64_t page = slot / a.block_size;
-    const int off = static_cast<int>(slot - page * a.block_size);
+// One thread per 16-element group; a warp takes whole tokens: 32 / groups-per-token tokens at
+// a time when a token has at most 32 groups (lane -> (token, group)), else one token with its
+// groups strided over the lanes.  Consecutive lanes read consecutive 64-byte groups
+// (coalesced), and the index arithmetic is 32-bit: the token's slot splits into (page,
+// offset) with one 32-bit division whenever the pool's slot count fits.
+__global__ void nvfp4_insert_kernel(QuantArgs a, int tpw) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int gpr = a.dim / 16;                // groups per row
+  const int gpt = a.rows_per_token * gpr;    // groups per token
+  const int span = tpw * gpt;                // groups per warp pass
+  const int64_t cap = a.num_pages * a.block_size;
+  const bool slots32 = cap <= 0x7fffffff;
+  for (int64_t t0 = warp * tpw; t0 < a.n_tokens; t0 += nwarps * tpw) {
+    for (int i = lane; i < span; i += 32) {
+      const int sub = i / gpt, gt = i - sub * gpt;
+      const int64_t tok = t0 + sub;
+      if (tok >= a.n_tokens) continue;
+      const int row = gt / gpr, grp = gt - row * gpr;
+      // the group's 64 input bytes do not depend on the slot: both loads go out together
+      const int64_t slot = __ldg(a.slots + tok);
+      const float4* src = reinterpret_cast<const float4*>(a.x + (tok * a.rows_per_token + row) * a.dim + grp * 16);
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 f = __ldg(src + j);
+        v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+      }
+      if (slot < 0 || slot >= cap) continue;
+      int64_t page;
+      int off;
+      if (slots32) {
+        const uint32_t s32 = static_cast<uint32_t>(slot), bs = static_cast<uint32_t>(a.block_size);
+        const uint32_t p32 = s32 / bs;
+        page = p32;
+        off = static_cast<int>(s32 - p32 * bs);
+      } else {
+        page = slot / a.block_size;
+        off = static_cast<int>(slot - page * a.block_size);
+      }
 
-    const float4* src = reinterpret_cast<const float4*>(a.x + (tok * a.rows_per_token + row) * a.dim + grp * 16);
-    float v[16];
+      float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float4 f = src[i];
-      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      const uint32_t scode = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
+      const float scale = e4m3_to_f32(scode);
+      uint2 packed = make_uint2(0u, 0u);
+      if (scale > 0.0f) {
+        float r[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = __fdiv_rn(v[j], scale);
+        packed.x = f32x8_to_e2m1x8(r);
+        packed.y = f32x8_to_e2m1x8(r + 8);
+      }
+      const int64_t row_index = (page * a.rows_per_token + row) * a.block_size + off;
+      *reinterpret_cast<uint2*>(a.data + row_index * (a.dim / 2) + grp * 8) = packed;
+      a.scale[row_index * gpr + grp] = static_cast<uint8_t>(scode);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const uint32_t scode = f32_to_e4m3(__fdiv_rn(amax, 6.0f));
-    const float scale = e4m3_to_f32(scode);
-    uint2 packed = make_uint2(0u, 0u);
-    if (scale > 0.0f) {
-      float r[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(v[i], scale);
-      packed.x = f32x8_to_e2m1x8(r);
-      packed.y = f32x8_to_e2m1x8(r + 8);
-    }
-    const int64_t row_index = (page * a.rows_per_token + row) * a.block_size + off;
-    *reinterpret_cast<uint2*>(a.data + row_index * (a.dim / 2) + grp * 8) = packed;
-    a.scale[row_index * groups_per_row + grp] = static_cast<uint8_t>(scode);
   }
 }
 
@@ -87,11 +107,13 @@ __global__ void fp8_quantize_kernel(const float* __restrict__ x, int64_t n, uint
 }
 
 cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s) {
-  const int64_t total = a.n_tokens * a.rows_per_token * (a.dim / 16);
-  if (total == 0) return cudaSuccess;
+  if (a.n_tokens == 0) return cudaSuccess;
+  const int gpt = a.rows_per_token * (a.dim / 16);
+  const int tpw = gpt >= 32 ? 1 : 32 / gpt;  // tokens per warp pass
   const int threads = 256;
-  const int64_t blocks = (total + threads - 1) / threads;
-  nvfp4_insert_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0, s>>>(a);
+  const int64_t warps = (a.n_tokens + tpw - 1) / tpw;
+  const int64_t blocks = (warps + threads / 32 - 1) / (threads / 32);
+  nvfp4_insert_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0, s>>>(a, tpw);
   return cudaGetLastError();
 }
 
