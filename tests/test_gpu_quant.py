@@ -19,6 +19,9 @@ def _edge_rows(rng, n, dim):
     x[5, :16] = np.concatenate([mids, -mids])
     x[6, :16] = np.concatenate([mids, -mids]) * np.float32(2.0 ** -7)
     x[7, :] = np.float32(448 * 6 * 1.01)
+    # infinite elements: the scale saturates at 448, the infinity at +-6, the rest keep their signs
+    x[8, :16] = np.float32([np.inf, -3.0, 1.0, -0.0, 2.0e3, -2.0e4, 5.0, 0.5] * 2)
+    x[9, 16:32] = np.float32([-np.inf, 3.0, -1.0, 0.0, -2.0e3, 2.0e4, -5.0, 7.0e5] * 2)
     return x
 
 
