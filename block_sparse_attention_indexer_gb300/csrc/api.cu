@@ -96,7 +96,8 @@ float scale_log2(const msa_config_t* c) {
 
 msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
-// stage 1: the streaming decode indexer, or its tcgen05 GEMM form for long query chunks
+// stage 1: the streaming decode indexer (<= 8 query rows per sequence), the tcgen05 form with
+// the keys as M (speculative decode, 9..63 rows) or the tcgen05 GEMM (long query chunks)
 cudaError_t run_indexer(const IndexerArgs& a, int sms, cudaStream_t s) {
   const int rows = a.q_len * a.groups;
   if (rows >= kPrefillMinRows) return launch_prefill_indexer(a, s);

@@ -163,8 +163,12 @@ msa_status_t msa_fp8_quantize(const float* x, int64_t n, uint8_t* out, void* str
  * visible keys j of block n of (qi[b][t][g] . key_j), exact products (E2M1 x E4M3 x E4M3)
  * accumulated in float32 (the log-sum-exp with expf / logf); -inf where block n has no
  * visible key (n beyond the query's own block or past the sequence end).  Entries
- * n >= ceil(seq_len/128) are written -inf too.  Any q_len works; q_len <= 8 takes the
- * decode kernel, larger q_len the prefill kernel.
+ * n >= ceil(seq_len/128) are written -inf too.  Any q_len works: with R = q_len x groups
+ * query rows per sequence, R <= 8 (decode) takes a streaming kernel, 8 < R < 64
+ * (speculative decode) a tcgen05 kernel with the keys as M, R >= 64 (chunked prefill) a
+ * tcgen05 GEMM with the query rows as M; all three give the same exact products and float32
+ * accumulation.  Errors: MSA_ERR_CUDA also when the driver's tensor-map encoder is not
+ * available (8 < R < 64) or num_pages * 128 exceeds 2^31 rows there.
  * workspace: msa_workspace_bytes(MSA_OP_INDEXER_SCORES, ...). */
 msa_status_t msa_indexer_scores(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                                 const uint8_t* index_q, float* block_scores, void* workspace,
