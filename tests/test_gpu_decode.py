@@ -107,11 +107,12 @@ def test_deterministic_reruns():
         assert np.array_equal(x, y, equal_nan=True)
 
 
-@pytest.mark.parametrize("T", [2, 80], ids=["t2", "t80_block_major"])
+@pytest.mark.parametrize("T", [2, 8, 80], ids=["t2", "t8_speculative", "t80_block_major"])
 def test_padding_rows_and_bad_inputs_flag_errors(T):
     """Padding rows, a length below q_len and a bad page: flagged, defined outputs, no fault --
-    for two query tokens and for 80 (the tcgen05 prefill indexer and the block-major plan,
-    which must skip the bad page's entries)."""
+    for two query tokens, for eight (32 query rows: the speculative tcgen05 indexer, whose bad
+    page is never copied and whose block scores there are -inf) and for 80 (the tcgen05
+    prefill indexer and the block-major plan, which must skip the bad page's entries)."""
     need_gpu()
     import torch
     import block_sparse_attention_indexer_gb300 as msa
