@@ -18,12 +18,13 @@
 //     shared memory), and one thread of warp 9 issues tcgen05.mma (A from TMEM: M 128 keys x N
 //     rows x K 16, eight per page) into one of two TMEM accumulators;
 //   * the epilogue warps (TMEM lane quarter = warp) load their 32 keys' scores 16 rows at a
-//     time and reduce over keys with a butterfly that transposes as it goes (four steps within
-//     each half-warp, one across: 16 shuffles leave lane c with the maximum of row c over the
-//     warp's keys); the causal mask is applied only on pages holding a key some row must not
-//     see.  Max pooling combines the four warps' maxima with integer atomics on an
-//     order-preserving encoding, so the warps never wait on each other; log-sum-exp pooling
-//     runs a second butterfly over e^{s - max} and combines through shared memory;
+//     time; the causal mask is applied only on pages holding a key some row must not see.
+//     Max pooling reduces each row over the warp's keys with one warp-wide f32 max
+//     (redux.sync), stages the 16 maxima so that lane j holds row j, and combines the four
+//     warps with integer atomics on an order-preserving encoding, so the warps never wait on
+//     each other.  Log-sum-exp pooling reduces with a butterfly that transposes as it goes
+//     (31 shuffles leave lane c with row c over the warp's keys), sums e^{s - max} the same
+//     way and combines through shared memory;
 //   * 10 warps, ~66 KB of shared memory and 256 TMEM columns: two CTAs share an SM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -57,6 +58,7 @@ struct SpShared {
   float red[2][4][kSpMaxN];   // per accumulator stage: each epilogue warp's per-row maxima
   float red2[2][4][kSpMaxN];  // the same for the log-sum-exp sums
   float sbuf[kSpMaxN][kSpKbMax + 1];
+  alignas(16) float wmax[4][16];  // max pooling: each epilogue warp's 16 column maxima of a chunk
 };
 
 // query tile | raw pages | shared
@@ -117,20 +119,11 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// The same over 16 values: lane l ends with the maximum of value l & 15 over all 32 lanes
-// (four transposing steps within each half-warp, then one plain step across the halves).
-__device__ __forceinline__ float transpose_max16(float (&v)[16], int lane) {
-#pragma unroll
-  for (int s = 8; s >= 1; s >>= 1) {
-    const bool upper = (lane & s) != 0;
-#pragma unroll
-    for (int i = 0; i < s; ++i) {
-      const float keep = upper ? v[i + s] : v[i];
-      const float send = upper ? v[i] : v[i + s];
-      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, s));
-    }
-  }
-  return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
+// Maximum of v over the warp's 32 lanes, in every lane (redux.sync on f32, sm_100 family)
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 // Order-preserving map of a float onto a signed int (negative values have their magnitude
@@ -358,14 +351,25 @@ __global__ void __launch_bounds__(kSpWarps * 32, 2) spec_indexer_kernel(const In
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] = (c0 + j >= cmin) ? v[j] : -INFINITY;
             }
-            const float m = transpose_max16(v, lane);  // row c0 + (lane & 15), this warp's keys
+            // the 16 columns' maxima over this warp's keys (warp-wide reductions), staged so that
+            // lane j holds column c0 + j
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = warp_max_f32(v[j]);
+            float* wm = sh->wmax[warp];
+            if (lane == 0) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(wm + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+            __syncwarp();
+            const float m = wm[lane & 15];
+            __syncwarp();  // every lane has read before the next chunk restages
             const int c = c0 + lane;
             if (lane < 16 && c < rows) atomicMax(&sbi[c * (kSpKbMax + 1) + k], ord_enc(m));
           }
         }
       } else {
-        // (every iteration reaches the named barrier below, also after a timed-out wait: a warp
-        // that left the loop would stall the others there)
+        // log-sum-exp pooling (every iteration reaches the named barrier below, also after a
+        // timed-out wait: a warp that left the loop would stall the others there)
         for (int k = 0; k < nblk; ++k) {
           const int acc = k & 1;
           if (!failed && !mbar_wait_warp(&sh->acc_full[acc], (k / 2) & 1)) failed = true;
@@ -384,28 +388,24 @@ __global__ void __launch_bounds__(kSpWarps * 32, 2) spec_indexer_kernel(const In
               if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
             }
             float v[32];
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int c = c0 + j;
               v[j] = (c < rows && c >= cmin) ? __uint_as_float(raw32[j]) : -INFINITY;
             }
-            if (!LSE) {
-              sh->red[acc][warp][c0 + lane] = transpose_reduce32<false>(v, lane);
-            } else {
-              float m32[32];
-  #pragma unroll
-              for (int j = 0; j < 32; ++j) m32[j] = v[j];
-              const float mlane = transpose_reduce32<false>(m32, lane);  // row c0 + lane, this warp's keys
-              sh->red[acc][warp][c0 + lane] = mlane;
-              // e^{s - m_w} with the row's maximum over this warp's keys; the rows' final maximum
-              // M is applied below: sum_j e^{s_j - m_w} e^{m_w - M} = sum_j e^{s_j - M}
-  #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float mw = __shfl_sync(0xffffffffu, mlane, j);
-                v[j] = (mw == -INFINITY) ? 0.f : expf(v[j] - mw);
-              }
-              sh->red2[acc][warp][c0 + lane] = transpose_reduce32<true>(v, lane);
+            float m32[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) m32[j] = v[j];
+            const float mlane = transpose_reduce32<false>(m32, lane);  // row c0 + lane, this warp's keys
+            sh->red[acc][warp][c0 + lane] = mlane;
+            // e^{s - m_w} with the row's maximum over this warp's keys; the rows' final maximum
+            // M is applied below: sum_j e^{s_j - m_w} e^{m_w - M} = sum_j e^{s_j - M}
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float mw = __shfl_sync(0xffffffffu, mlane, j);
+              v[j] = (mw == -INFINITY) ? 0.f : expf(v[j] - mw);
             }
+            sh->red2[acc][warp][c0 + lane] = transpose_reduce32<true>(v, lane);
           }
           if (failed) {  // defined values for the reduction below
             sh->red[acc][warp][lane] = -INFINITY;
@@ -416,11 +416,11 @@ __global__ void __launch_bounds__(kSpWarps * 32, 2) spec_indexer_kernel(const In
           if (warp == 0) {
             for (int c = lane; c < rows; c += 32) {
               float m = -INFINITY;
-  #pragma unroll
+#pragma unroll
               for (int w = 0; w < 4; ++w) m = fmaxf(m, sh->red[acc][w][c]);
-              if (LSE && m != -INFINITY) {
+              if (m != -INFINITY) {
                 float sum = 0.f;
-  #pragma unroll
+#pragma unroll
                 for (int w = 0; w < 4; ++w) {
                   const float mw = sh->red[acc][w][c];
                   if (mw != -INFINITY) sum += sh->red2[acc][w][c] * expf(mw - m);
