@@ -368,7 +368,7 @@ def run_ours(args):
     d_q, d_qi, d_table, d_lens = (view(d_stage, o, s_) for s_, o in zip(src, offs))
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e_batch = msa.Batch(d_table, d_lens, T)
-    h2d = sum(s_.numel() * s_.element_size() for s_ in src)
+    h2d = h_stage.numel()  # the bytes the copy moves: the inputs plus their 256-byte alignment padding
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
