@@ -212,7 +212,8 @@ class OracleSample:
             t_total += time.perf_counter() - t0
             done.append(b)
             k += 1
-        return rows / t_total, {"sequences": done, "query_rows": rows, "seconds": round(t_total, 3)}
+        return rows / t_total, {"sequences": sorted(set(done)), "sequence_runs": len(done), "query_rows": rows,
+                                "seconds": round(t_total, 3)}
 
 
 def run_reference(args):
