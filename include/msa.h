@@ -62,7 +62,7 @@ extern "C" {
 typedef enum {
   MSA_OK = 0,
   MSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
-  MSA_ERR_UNSUPPORTED = 2,  /* a configuration this build does not implement */
+  MSA_ERR_UNSUPPORTED = 2,  /* a configuration the library does not implement */
   MSA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than msa_workspace_bytes() */
   MSA_ERR_CUDA = 4          /* a CUDA launch or query failed */
 } msa_status_t;
@@ -81,7 +81,7 @@ typedef enum {
 /* Sparse configuration.  The pages' M3 recipe: block 128, top-16, init_blocks = 0,
  * local_blocks = 1, max pooling ("MiniMax M3 x vLLM：百万 token 多模态推理的 Day-0 部署",
  * §MSA 机制细节, which names init_blocks / local_blocks as configuration).
- * This build implements: num_kv_groups in 1..8, heads_per_group in 1..8,
+ * The library implements: num_kv_groups in 1..8, heads_per_group in 1..8,
  * head_dim = index_dim = block_size = 128, 1 <= top_k <= 16, init_blocks >= 0,
  * local_blocks >= 0 with init_blocks + local_blocks <= top_k, score_type MSA_SCORE_MAX or
  * MSA_SCORE_LSE; anything else returns MSA_ERR_UNSUPPORTED.
