@@ -30,9 +30,12 @@ def _run_decode(dw):
 
 
 def _check(w, dw, sequences=None, tokens=None):
+    """msa_decode's scores, selections, outputs and lse against the oracle on the given
+    sequences x tokens (default: all).  The oracle quantises the index keys of those
+    sequences and, for the attention, K and V of the blocks its own selection picks."""
     out, lse, sel, scores = _run_decode(dw)
     seqs = list(range(w.batch)) if sequences is None else list(sequences)
-    cache, table, lens, P = OC.build_cache(w, dw.lens, seqs, threads=16)
+    cache, table, lens, P = OC.build_cache(w, dw.lens, seqs, threads=16, index_only=True)
     q, qi = OC.encode_queries(w, seqs)
     toks = list(range(w.q_len)) if tokens is None else list(tokens)
     ref_s = OM.block_scores(qi, cache[4], cache[5], table, lens, tokens=toks, sequences=seqs)
@@ -48,6 +51,7 @@ def _check(w, dw, sequences=None, tokens=None):
             for g in range(4):
                 ref_sel[b, t, g] = OM.select_row(ref_s[b, t, g], L - w.q_len + t)
     diff = selection_diffs(np.where(rows[:, :, None, None], sel, -1), ref_sel, ref_s, lens, w.q_len)
+    OC.add_kv_blocks(cache, w, table, {(b, int(n)) for b in seqs for n in ref_sel[b].ravel() if n >= 0}, threads=16)
     out_ref, lse_ref = OM.sparse_attention(q, *cache[:4], table, lens, ref_sel, w.heads_per_group, tokens=toks,
                                            sequences=seqs)
     mask = rows.copy()
@@ -71,28 +75,34 @@ def test_b8_32k_full():
     _check(w, device_workload(w))
 
 
-def test_ragged64_128k_sampled():
+def test_ragged64_128k_full():
+    """The headline workload, every one of its 64 sequences (4.6 M cached tokens)."""
     need_gpu()
     w = syn.WORKLOADS["ragged64_128k"]
-    dw = device_workload(w)
-    lens = dw.lens
-    picks = sorted({int(np.argmax(lens)), int(np.argmin(lens)), 17, 42})
-    _check(w, dw, sequences=picks)
+    _check(w, device_workload(w))
 
 
-def test_spec4_512k_sampled():
+def test_spec4_512k_full():
+    """Speculative decode, all 4 sequences x 8 query tokens."""
     need_gpu()
     w = syn.WORKLOADS["spec4_512k"]
-    dw = device_workload(w)
-    _check(w, dw, sequences=[2])
+    _check(w, device_workload(w))
 
 
 def test_prefill_4k_on_64k_sampled():
+    """Chunked prefill on 520 of the 4,096 new tokens: the first and last token of every
+    128-token block the chunk covers, plus a seeded sample of the rest."""
     need_gpu()
     w = syn.WORKLOADS["prefill_4k_on_64k"]
     dw = device_workload(w)
+    T = w.q_len
+    pos0 = int(dw.lens[0]) - T
+    edges = {t for t in range(T) if (pos0 + t) % 128 in (0, 127)}
     rng = np.random.default_rng(0)
-    toks = sorted(set(range(8)) | set(range(4088, 4096)) | set(int(x) for x in rng.choice(4096, 24, replace=False)))
+    rest = [t for t in range(T) if t not in edges]
+    toks = sorted(edges | {0, T - 1} | set(int(x) for x in rng.choice(rest, 520 - len(edges | {0, T - 1}),
+                                                                        replace=False)))
+    assert len(toks) == 520
     _check(w, dw, tokens=toks)
 
 

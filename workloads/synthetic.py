@@ -102,19 +102,31 @@ def layout(w: Workload, lens: np.ndarray | None = None):
     return num_pages, table, lens
 
 
+def gen_index_block_fp32(w: Workload, b: int, n: int) -> np.ndarray:
+    """fp32 index keys of block n of sequence b, [128, Di], with the block's offset vector."""
+    idx = _normal(_philox(w.seed, KIND_IDX, b, n), (BLOCK, INDEX_DIM))
+    off = _normal(_philox(w.seed, KIND_OFFSET, b, n), (INDEX_DIM,)) * np.float32(w.offset_std)
+    idx += off[None, :]
+    return idx
+
+
+def gen_kv_block_fp32(w: Workload, b: int, n: int):
+    """fp32 K and V of block n of sequence b, each [128, G, D]."""
+    k = _normal(_philox(w.seed, KIND_K, b, n), (BLOCK, NUM_KV_GROUPS, HEAD_DIM))
+    v = _normal(_philox(w.seed, KIND_V, b, n), (BLOCK, NUM_KV_GROUPS, HEAD_DIM))
+    return k, v
+
+
 def gen_block_fp32(w: Workload, b: int, n: int):
     """fp32 values of block n of sequence b.
 
     Returns (k [128, G, D], v [128, G, D], idx [128, Di]); the index keys already carry the
     block's offset vector.  Tokens past the sequence end are generated too (they are never
-    visible to any query).
+    visible to any query).  Each tensor has its own stream, so the parts can be drawn alone
+    (gen_index_block_fp32, gen_kv_block_fp32) with the same values.
     """
-    k = _normal(_philox(w.seed, KIND_K, b, n), (BLOCK, NUM_KV_GROUPS, HEAD_DIM))
-    v = _normal(_philox(w.seed, KIND_V, b, n), (BLOCK, NUM_KV_GROUPS, HEAD_DIM))
-    idx = _normal(_philox(w.seed, KIND_IDX, b, n), (BLOCK, INDEX_DIM))
-    off = _normal(_philox(w.seed, KIND_OFFSET, b, n), (INDEX_DIM,)) * np.float32(w.offset_std)
-    idx += off[None, :]
-    return k, v, idx
+    k, v = gen_kv_block_fp32(w, b, n)
+    return k, v, gen_index_block_fp32(w, b, n)
 
 
 def gen_queries(w: Workload, b: int) -> np.ndarray:
@@ -144,6 +156,7 @@ def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-__all__ = ["WORKLOADS", "Workload", "seq_lens", "layout", "gen_block_fp32", "gen_queries",
+__all__ = ["WORKLOADS", "Workload", "seq_lens", "layout", "gen_block_fp32", "gen_index_block_fp32",
+           "gen_kv_block_fp32", "gen_queries",
            "gen_index_queries", "custom", "BLOCK", "HEAD_DIM", "INDEX_DIM", "NUM_KV_GROUPS", "TOP_K",
            "total_tokens", "ceil_div"]
