@@ -25,10 +25,12 @@ from .binding import (  # noqa: F401
     msa_decode,
     msa_fp8_quantize,
     msa_indexer_scores,
+    msa_noalloc_read_device_error,
     msa_nvfp4_insert,
     msa_read_device_error,
     msa_select_blocks,
     msa_sparse_attn_decode,
     msa_sparse_attn_decode_noalloc,
+    msa_test_indexer_stall,
     msa_workspace_bytes,
 )

@@ -64,6 +64,8 @@ _SIGS = {
     "msa_sparse_attn_decode": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msa_decode": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msa_sparse_attn_decode_noalloc": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P]),
+    "msa_noalloc_read_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _P]),
+    "msa_test_indexer_stall": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     "msa_read_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "msa_clear_device_error": (ctypes.c_int, [_P, _P]),
 }
@@ -239,6 +241,23 @@ def msa_sparse_attn_decode_noalloc(cfg: Config, cache: PagedCache, batch: Batch,
     _check("msa_sparse_attn_decode_noalloc", _lib.msa_sparse_attn_decode_noalloc(
         cfg.c(), cache.c(), batch.c(), _ptr(q, torch.uint8, "q"), _ptr(selection, torch.int32, "selection"),
         _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream)))
+
+
+def msa_noalloc_read_device_error(stream=None) -> int:
+    """The device error word of the no-allocation entry point's array (the last call's)."""
+    flags = ctypes.c_uint32(0)
+    _check("msa_noalloc_read_device_error", _lib.msa_noalloc_read_device_error(ctypes.byref(flags), _stream(stream)))
+    return int(flags.value)
+
+
+def msa_test_indexer_stall(cfg: Config, cache: PagedCache, batch: Batch, index_q: torch.Tensor,
+                           block_scores: torch.Tensor, workspace: torch.Tensor, spin_limit: int, stream=None):
+    """Test hook: the streaming indexer with its page copies withheld and its waits capped at
+    spin_limit polls (include/msa.h)."""
+    _check("msa_test_indexer_stall", _lib.msa_test_indexer_stall(
+        cfg.c(), cache.c(), batch.c(), _ptr(index_q, torch.uint8, "index_q"),
+        _ptr(block_scores, torch.float32, "block_scores"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), spin_limit, _stream(stream)))
 
 
 def msa_decode(cfg: Config, cache: PagedCache, batch: Batch, q: torch.Tensor, index_q: torch.Tensor,

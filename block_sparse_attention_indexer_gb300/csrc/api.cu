@@ -89,6 +89,8 @@ size_t attn_scratch_bytes(const msa_config_t* c, const msa_batch_t* b) {
              : partial_bytes();
 }
 
+
+
 float scale_log2(const msa_config_t* c) {
   const float sm = c->softmax_scale > 0.0f ? c->softmax_scale : 1.0f / std::sqrt(static_cast<float>(c->head_dim));
   return sm * 1.4426950408889634f;
@@ -121,6 +123,7 @@ IndexerArgs indexer_args(const msa_config_t* cfg, const msa_cache_t* cache, cons
   a.block_scores = scores;
   a.err = err;
   a.lse = cfg->score_type == MSA_SCORE_LSE ? 1 : 0;
+  a.spin_limit = kDefaultSpinLimit;
   return a;
 }
 
@@ -161,6 +164,7 @@ AttnArgs attn_args(const msa_config_t* cfg, const msa_cache_t* cache, const msa_
   a.partial = partial;
   a.scale_log2 = scale_log2(cfg);
   a.err = err;
+  a.spin_limit = kDefaultSpinLimit;
   return a;
 }
 
@@ -180,7 +184,8 @@ size_t msa::team_attn_workspace_bytes() { return kErrBytes + partial_bytes(); }
 
 msa_status_t msa::sparse_attn_entry(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                                     const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
-                                    void* workspace, size_t workspace_bytes, void* stream, bool block_major_ok) {
+                                    void* workspace, size_t workspace_bytes, void* stream, bool block_major_ok,
+                                    bool clear_error) {
   msa_status_t st;
   if ((st = check_config(cfg)) != MSA_OK || (st = check_batch(batch)) != MSA_OK ||
       (st = check_cache(cache, false, true)) != MSA_OK)
@@ -194,6 +199,8 @@ msa_status_t msa::sparse_attn_entry(const msa_config_t* cfg, const msa_cache_t* 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   AttnArgs a = attn_args(cfg, cache, batch, q, selection, out, lse, reinterpret_cast<float*>(ws + kErrBytes),
                          reinterpret_cast<uint32_t*>(ws));
+  if (clear_error && cudaMemsetAsync(ws, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MSA_ERR_CUDA;
   return cuda_status(run_attention(cfg, batch, a, ws + kErrBytes, sms, static_cast<cudaStream_t>(stream), block_major_ok));
 }
 
@@ -289,7 +296,8 @@ msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch
 msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                                     const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
                                     void* workspace, size_t workspace_bytes, void* stream) {
-  return msa::sparse_attn_entry(cfg, cache, batch, q, selection, out, lse, workspace, workspace_bytes, stream, true);
+  return msa::sparse_attn_entry(cfg, cache, batch, q, selection, out, lse, workspace, workspace_bytes, stream, true,
+                                false);
 }
 
 msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
@@ -321,6 +329,28 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
   aa.q_early = 1;  // the kernel before it is this step's selection
   if (e == cudaSuccess) e = run_attention(cfg, batch, aa, scratch, sms, s, true);
   return cuda_status(e);
+}
+
+msa_status_t msa_test_indexer_stall(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                    const uint8_t* index_q, float* block_scores, void* workspace,
+                                    size_t workspace_bytes, uint32_t spin_limit, void* stream) {
+  msa_status_t st;
+  if ((st = check_config(cfg)) != MSA_OK || (st = check_batch(batch)) != MSA_OK ||
+      (st = check_cache(cache, true, false)) != MSA_OK)
+    return st;
+  if (batch->batch == 0) return MSA_OK;
+  if (batch->q_len * cfg->num_kv_groups > 8 || spin_limit < 1 || spin_limit > kDefaultSpinLimit)
+    return MSA_ERR_UNSUPPORTED;
+  if (index_q == nullptr || block_scores == nullptr || !aligned16(index_q)) return MSA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < msa_workspace_bytes(MSA_OP_INDEXER_SCORES, cfg, batch) ||
+      !aligned16(workspace))
+    return MSA_ERR_WORKSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MSA_ERR_CUDA;
+  IndexerArgs a = indexer_args(cfg, cache, batch, index_q, block_scores, static_cast<uint32_t*>(workspace));
+  a.spin_limit = spin_limit;
+  a.test_withhold = 1;
+  return cuda_status(launch_indexer(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 msa_status_t msa_read_device_error(const void* workspace, uint32_t* flags, void* stream) {

@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "attention_tile.cuh"
 #include "msa_device.cuh"
 #include "msa_kernels.h"
 
@@ -39,20 +40,6 @@ constexpr int kTW = 4;                                    // warps per team (one
 constexpr int kAW = kTeams * kTW;                         // consuming warps per CTA
 constexpr int kAttnThreads = (kAW + kTeams) * 32;         // + one producer warp per team
 constexpr int kTSl = 3;                                   // page slots per team
-constexpr int kSlotBytes = 2 * (kPageData + kPageScale);  // K data | K scales | V data | V scales
-constexpr int kHeadsMax = 8;
-constexpr int kRedFloats = kHeadsMax * kDim + 2 * kHeadsMax;   // one warp's o[8][128], m[8], l[8]
-constexpr int kSlotFloats = kHeadsMax * (kDim + 2);             // one partial slot: [8][o 128, m, l]
-constexpr float kLn2 = 0.69314718055994530942f;
-
-// 2^x by the hardware approximation (ex2.approx, relative error about 2^-22), subnormal
-// results flushed to zero: softmax weights below 2^-126 of the row maximum count as 0.
-__device__ __forceinline__ float exp2_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // per team: slots, merge area, item metadata, barriers
 struct TeamBars {
   uint64_t full[kTSl];   // a page (or a marker item) is in the slot: 1 arrive (+ copy bytes)
@@ -113,7 +100,7 @@ __device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int row) {
 __device__ __forceinline__ bool send_item(const AttnArgs& a, int& produced, uint8_t* slots, ItemMeta* meta,
                                           TeamBars* tb, int lane, int row, int blk, int page, int pos) {
   const int slot = produced % kTSl;
-  if (produced >= kTSl && !mbar_wait_warp(&tb->empty[slot], ((produced / kTSl) - 1) & 1)) return false;
+  if (produced >= kTSl && !mbar_wait_warp(&tb->empty[slot], ((produced / kTSl) - 1) & 1, a.spin_limit)) return false;
   if (lane == 0) {
     uint64_t* bar = &tb->full[slot];
     meta[slot].row = row;
@@ -145,188 +132,6 @@ __device__ __forceinline__ bool send_item(const AttnArgs& a, int& produced, uint
   return true;
 }
 
-// The producer's view of one row, in two steps so that a row's loads can be in flight while
-// the row before it is being sent: row_fetch issues the loads that depend only on the row
-// (its selection, lane j < 16: block id of entry j, and its sequence length), row_resolve
-// then checks them and looks up the page of each entry (-1: empty, past the recent block,
-// or a bad block-table entry).
-struct RowRaw {
-  int blk, L;
-};
-
-__device__ __forceinline__ RowRaw row_fetch(const AttnArgs& a, int R, int lane) {
-  RowRaw raw;
-  raw.blk = lane < kTopK ? a.selection[static_cast<int64_t>(R) * kTopK + lane] : -1;
-  raw.L = a.seq_lens[static_cast<unsigned>(R) / static_cast<unsigned>(a.q_len * a.groups)];
-  return raw;
-}
-
-__device__ __forceinline__ void row_resolve(const AttnArgs& a, int R, const RowRaw& raw, int lane, int& blk,
-                                            int& page, int& pos) {
-  const unsigned TG = static_cast<unsigned>(a.q_len * a.groups);
-  const int b = static_cast<int>(static_cast<unsigned>(R) / TG);
-  const int t = static_cast<int>((static_cast<unsigned>(R) - static_cast<unsigned>(b) * TG) /
-                                 static_cast<unsigned>(a.groups));
-  const int L = raw.L;
-  const bool ok = L > 0 && L >= a.q_len && L <= static_cast<int64_t>(a.max_blocks) * kBlock;
-  pos = L - a.q_len + t;
-  const int r = ok ? pos / kBlock : -1;
-  blk = ok ? raw.blk : -1;
-  // the table lookup only needs an in-range block id; its validity comes from ok and r
-  int p = -1;
-  if (blk >= 0 && blk < a.max_blocks) p = a.block_table[static_cast<int64_t>(b) * a.max_blocks + blk];
-  page = -1;
-  if (blk >= 0 && blk <= r) {
-    if (p >= 0 && p < a.num_pages)
-      page = p;
-    else
-      flag_error(a.err, MSA_DEVERR_BAD_PAGE);
-  }
-}
-
-// The raw FP8 queries of head row gq of a group's row (lane: 32 bytes of dims 32 t4 ..).
-__device__ __forceinline__ void load_q_raw(const AttnArgs& a, int row, int gq, int t4, uint4& q0, uint4& q1) {
-  if (gq < a.heads_per_group) {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        a.q + (static_cast<int64_t>(row) * a.heads_per_group + gq) * kDim + 32 * t4);
-    q0 = __ldg(src);
-    q1 = __ldg(src + 1);
-  } else {
-    q0 = q1 = make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-__device__ __forceinline__ void q_fragments(const uint4& q0, const uint4& q1, uint32_t (&bq)[8][2]) {
-  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    bq[s][0] = e4m3x2_to_f16x2(w[s]);
-    bq[s][1] = e4m3x2_to_f16x2(w[s] >> 16);
-  }
-}
-
-// One 32-key quarter (qk) of one page (128 keys of one KV head) into the warp's state.
-__device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n, int r, int pos, float scale_log2,
-                                               int gq, int t4, const uint32_t (&bq)[8][2], float (&m_run)[2],
-                                               float (&l_run)[2], float (&o)[8][4]) {
-  const uint8_t* ks = kd + kPageData;
-  const uint8_t* vd = ks + kPageScale;
-  const uint8_t* vs = vd + kPageData;
-  const bool recent = (n == r);
-  // ---- S^T = K Q^T for 32 keys (two 16-key tiles), raw (unscaled) logits
-  float x[2][4];
-#pragma unroll
-  for (int mq = 0; mq < 2; ++mq) {
-    // tile row i holds key pi(i) = (i & 8) | (i & 1) << 2 | (i >> 1) & 3 of the 16: the PV
-    // step's lanes then read V rows 1 apart (2-way bank conflicts instead of 4-way)
-    const int r0 = qk * 32 + mq * 16 + (((gq & 1) << 2) | (gq >> 1)), r1 = r0 + 8;
-    const uint4 d0 = lds128(kd + r0 * kRowBytes + 16 * t4);
-    const uint4 d1 = lds128(kd + r1 * kRowBytes + 16 * t4);
-    // the lane's two block scales of each row, as f16 pairs (s, s)
-    const uint32_t f0 = e4m3x2_to_f16x2(lds16(ks + r0 * kRowScales + 2 * t4));
-    const uint32_t f1 = e4m3x2_to_f16x2(lds16(ks + r1 * kRowScales + 2 * t4));
-    const uint32_t sc0[2] = {__byte_perm(f0, 0, 0x1010), __byte_perm(f0, 0, 0x3232)};
-    const uint32_t sc1[2] = {__byte_perm(f1, 0, 0x1010), __byte_perm(f1, 0, 0x3232)};
-    const uint32_t w0[4] = {d0.x, d0.y, d0.z, d0.w};
-    const uint32_t w1[4] = {d1.x, d1.y, d1.z, d1.w};
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-      e2m1x8_to_f16x2(w0[w], x0, x1, x2, x3);
-      e2m1x8_to_f16x2(w1[w], y0, y1, y2, y3);
-      const uint32_t sa = sc0[w >> 1], sb = sc1[w >> 1];
-      x0 = hmul2(x0, sa); x1 = hmul2(x1, sa); x2 = hmul2(x2, sa); x3 = hmul2(x3, sa);
-      y0 = hmul2(y0, sb); y1 = hmul2(y1, sb); y2 = hmul2(y2, sb); y3 = hmul2(y3, sb);
-      mma_f16_16816(acc, x0, y0, x1, y1, bq[2 * w][0], bq[2 * w][1]);
-      mma_f16_16816(acc, x2, y2, x3, y3, bq[2 * w + 1][0], bq[2 * w + 1][1]);
-    }
-    const int j0 = n * kBlock + r0, j1 = j0 + 8;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) x[mq][e] = acc[e];
-    if (recent) {
-      if (j0 > pos) x[mq][0] = x[mq][1] = -INFINITY;
-      if (j1 > pos) x[mq][2] = x[mq][3] = -INFINITY;
-    }
-  }
-
-  // ---- online softmax per head column (2*t4 + e), in the exp2 domain: logit * scale_log2
-  // (the scale is positive, so the maximum of the raw logits scales to the running maximum)
-  float p[2][4], alpha[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    float mx = fmaxf(fmaxf(x[0][e], x[0][e + 2]), fmaxf(x[1][e], x[1][e + 2]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float m_new = fmaxf(m_run[e], mx * scale_log2);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    alpha[e] = exp2_ftz(m_run[e] - m_use);
-    m_run[e] = m_new;
-    float sum = 0.f;
-#pragma unroll
-    for (int mq = 0; mq < 2; ++mq) {
-      p[mq][e] = exp2_ftz(fmaf(x[mq][e], scale_log2, -m_use));
-      p[mq][e + 2] = exp2_ftz(fmaf(x[mq][e + 2], scale_log2, -m_use));
-      sum += p[mq][e] + p[mq][e + 2];
-    }
-    l_run[e] = l_run[e] * alpha[e] + sum;
-  }
-  // rescale the output only when some head's running maximum moved (warp-uniform test)
-  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= alpha[0];
-      o[mt][2] *= alpha[0];
-      o[mt][1] *= alpha[1];
-      o[mt][3] *= alpha[1];
-    }
-  }
-
-  // ---- O^T += V^T P^T, one 16-key k-step per QK tile
-#pragma unroll
-  for (int mq = 0; mq < 2; ++mq) {
-    const uint32_t b0 = movmatrix_trans(pack_f16x2(p[mq][0], p[mq][1]));
-    const uint32_t b1 = movmatrix_trans(pack_f16x2(p[mq][2], p[mq][3]));
-    // k-indices 2t4, 2t4+1, 2t4+8, 2t4+9 are keys pi(.) = t4, t4+4, t4+8, t4+12 of the tile
-    const int ka = qk * 32 + mq * 16 + t4;
-    const uint2 va = lds64(vd + ka * kRowBytes + 8 * gq);
-    const uint2 vb = lds64(vd + (ka + 4) * kRowBytes + 8 * gq);
-    const uint2 vc = lds64(vd + (ka + 8) * kRowBytes + 8 * gq);
-    const uint2 ve = lds64(vd + (ka + 12) * kRowBytes + 8 * gq);
-    const uint32_t sab = e4m3x2_to_f16x2(lds8(vs + ka * kRowScales + gq) |
-                                         (lds8(vs + (ka + 4) * kRowScales + gq) << 8));
-    const uint32_t scd = e4m3x2_to_f16x2(lds8(vs + (ka + 8) * kRowScales + gq) |
-                                         (lds8(vs + (ka + 12) * kRowScales + gq) << 8));
-#pragma unroll
-    for (int hw = 0; hw < 2; ++hw) {
-      const uint32_t wa = hw ? va.y : va.x, wb = hw ? vb.y : vb.x;
-      const uint32_t wc = hw ? vc.y : vc.x, we = hw ? ve.y : ve.x;
-      // byte i of lo*: low nibbles of (key a, key b); of hi*: their high nibbles
-      const uint32_t lo_ab = (wa & 0x0F0F0F0Fu) | ((wb & 0x0F0F0F0Fu) << 4);
-      const uint32_t hi_ab = ((wa >> 4) & 0x0F0F0F0Fu) | (wb & 0xF0F0F0F0u);
-      const uint32_t lo_ce = (wc & 0x0F0F0F0Fu) | ((we & 0x0F0F0F0Fu) << 4);
-      const uint32_t hi_ce = ((wc >> 4) & 0x0F0F0F0Fu) | (we & 0xF0F0F0F0u);
-      uint32_t la[4], ha[4], lc[4], hc[4];
-      e2m1x8_to_f16x2(lo_ab, la[0], la[1], la[2], la[3]);
-      e2m1x8_to_f16x2(hi_ab, ha[0], ha[1], ha[2], ha[3]);
-      e2m1x8_to_f16x2(lo_ce, lc[0], lc[1], lc[2], lc[3]);
-      e2m1x8_to_f16x2(hi_ce, hc[0], hc[1], hc[2], hc[3]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int mt = hw * 4 + i;  // output dims 16*gq + 2*mt (+1)
-        mma_f16_16816(o[mt], hmul2(la[i], sab), hmul2(ha[i], sab), hmul2(lc[i], scd), hmul2(hc[i], scd), b0, b1);
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void write_out(const AttnArgs& a, int head_row, int d, float num, float den, float M) {
-  const float v = den > 0.f ? num / den : 0.f;
-  a.out[static_cast<int64_t>(head_row) * kDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  if (d == 0 && a.lse != nullptr) a.lse[head_row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
-}
-
 __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   TeamBars* tbars = reinterpret_cast<TeamBars*>(smem + kSlotsBytes);
@@ -352,7 +157,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
   __syncthreads();
 
   // Launched as a programmatic dependent of the previous kernel on the stream (the
-  // selection): the prologue above, and on the fused decode path the consumers' first
+  // selection): the prologue above, and on the msa_decode path the consumers' first
   // queries below, run before that kernel has finished; everything that reads what it
   // writes comes after this wait.
   if (warp >= kAW) {
@@ -391,7 +196,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
     if (!ok) {
       if (lane == 0) flag_error(a.err, MSA_DEVERR_TIMEOUT);
       // wait (bounded) for the copies still in flight before leaving
-      for (int k = max(0, produced - kTSl); k < produced; ++k) mbar_wait(&tb->full[k % kTSl], (k / kTSl) & 1);
+      for (int k = max(0, produced - kTSl); k < produced; ++k)
+        mbar_wait(&tb->full[k % kTSl], (k / kTSl) & 1, a.spin_limit);
     }
     return;
   }
@@ -422,7 +228,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
       v += __shfl_xor_sync(0xffffffffu, v, 16);
       l_run[e] = v;
     }
-    if (nseg > 0 && !mbar_wait_warp(&tb->freed, (nseg - 1) & 1)) return false;
+    if (nseg > 0 && !mbar_wait_warp(&tb->freed, (nseg - 1) & 1, a.spin_limit)) return false;
     float* my_red = team_red + wt * kRedFloats;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -438,7 +244,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&tb->merged);
-    if (!mbar_wait_warp(&tb->merged, nseg & 1)) return false;
+    if (!mbar_wait_warp(&tb->merged, nseg & 1, a.spin_limit)) return false;
     const bool whole = R * kTopK >= x0 && (R + 1) * kTopK <= x1;
     float* slot_part = whole ? nullptr : a.partial + static_cast<int64_t>(2 * tt + (R == R0 ? 0 : 1)) * kSlotFloats;
     // lane (w, h) = (lane >> 3, lane & 7): weight e^{m_w - M} of warp w's state for head h,
@@ -459,7 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
       for (int w = 0; w < kTW; ++w) num += __shfl_sync(0xffffffffu, fw, w * 8 + h) * team_red[w * kRedFloats + h * kDim + d];
       const float M = __shfl_sync(0xffffffffu, Mh, h), dh = __shfl_sync(0xffffffffu, den, h);
       if (whole) {
-        write_out(a, R * Hg + h, d, num, dh, M);
+        write_out(a.out, a.lse, R * Hg + h, d, num, dh, M);
       } else {
         slot_part[h * (kDim + 2) + d] = num;
         if (d == 0) {
@@ -482,14 +288,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
   int q_row = -1;
   if (!a.q_early) grid_dependency_wait();
   if (x0 < x1) {
-    load_q_raw(a, R0, gq, t4, qn0, qn1);
+    load_q_raw(a.q, a.heads_per_group, R0, gq, t4, qn0, qn1);
     q_row = R0;
   }
   if (a.q_early) grid_dependency_wait();
   grid_dependents_launch();
   while (true) {
     const int slot = consumed % kTSl;
-    if (!mbar_wait_warp(&tb->full[slot], (consumed / kTSl) & 1)) {
+    if (!mbar_wait_warp(&tb->full[slot], (consumed / kTSl) & 1, a.spin_limit)) {
       failed = true;
       break;
     }
@@ -503,10 +309,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
         break;
       }
       if (row >= 0) {
-        if (q_row != row) load_q_raw(a, row, gq, t4, qn0, qn1);
+        if (q_row != row) load_q_raw(a.q, a.heads_per_group, row, gq, t4, qn0, qn1);
         q_fragments(qn0, qn1, bq);
         if ((row + 1) * kTopK < x1) {
-          load_q_raw(a, row + 1, gq, t4, qn0, qn1);
+          load_q_raw(a.q, a.heads_per_group, row + 1, gq, t4, qn0, qn1);
           q_row = row + 1;
         }
         m_run[0] = m_run[1] = -INFINITY;
@@ -593,8 +399,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a, 
     }
   }
   const int head_row = R * a.heads_per_group + h;
-  write_out(a, head_row, d, num0, den, M);
-  write_out(a, head_row, d + 1, num1, den, M);
+  write_out(a.out, a.lse, head_row, d, num0, den, M);
+  write_out(a.out, a.lse, head_row, d + 1, num1, den, M);
 }
 
 size_t attn_partial_bytes() {

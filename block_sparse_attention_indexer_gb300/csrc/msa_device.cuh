@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "../../include/msa.h"
+#include "msa_kernels.h"
 
 namespace msa {
 
@@ -17,7 +18,7 @@ constexpr int kRowScales = kDim / 16;          // E4M3 scales per row
 constexpr int kPageData = kBlock * kRowBytes;  // 8192
 constexpr int kPageScale = kBlock * kRowScales;// 1024
 constexpr int kTopK = 16;
-constexpr uint32_t kSpinLimit = 1u << 22;      // bound on every mbarrier wait loop
+constexpr uint32_t kSpinLimit = kDefaultSpinLimit;  // default bound on every mbarrier wait loop
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
@@ -143,9 +144,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on one phase; false if it gave up (the caller flags MSA_DEVERR_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Bounded wait on one phase: at most `limit` polls; false if it gave up (the caller flags
+// MSA_DEVERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -153,8 +155,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // The same, called by a whole warp; the verdict is made warp-uniform so that the warp's
 // later shuffles never diverge.  (Every lane waits: a variant where lane 0 alone polls and
 // broadcasts was measured slower, its divergent loop costing more than the shared polls.)
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t limit = kSpinLimit) {
+  const bool ok = mbar_wait(bar, parity, limit);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 

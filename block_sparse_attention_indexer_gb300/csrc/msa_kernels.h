@@ -8,6 +8,10 @@
 
 namespace msa {
 
+// Polls every bounded wait makes before it gives up and flags MSA_DEVERR_TIMEOUT (kernels
+// whose arguments carry a spin_limit take it from there).
+constexpr uint32_t kDefaultSpinLimit = 1u << 22;
+
 struct IndexerArgs {
   const uint8_t* idx_data;     // [P][128][64]
   const uint8_t* idx_scale;    // [P][128][8]
@@ -19,6 +23,8 @@ struct IndexerArgs {
   float* block_scores;         // [B][T][G][max_blocks]
   uint32_t* err;
   int32_t lse;                 // block pooling: 0 max, 1 log-sum-exp
+  uint32_t spin_limit;         // polls per bounded wait (streaming kernel)
+  int32_t test_withhold;       // test hook: the streaming kernel issues no page copies
 };
 
 struct SelectArgs {
@@ -47,6 +53,7 @@ struct AttnArgs {
   float scale_log2;            // softmax_scale * log2(e)
   int32_t q_early;             // 1: read the first queries before waiting on the previous kernel
   uint32_t* err;
+  uint32_t spin_limit;         // polls per bounded wait (team kernel)
 };
 
 struct QuantArgs {

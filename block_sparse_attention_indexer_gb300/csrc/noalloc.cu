@@ -10,7 +10,9 @@
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes (8 MiB).  Every GPU
 // that loads the library holds it until the process exits.  In host code the array's name is
 // only a host-side stand-in, so the device address is looked up with cudaGetSymbolAddress,
-// once per device, with that device current, on the first call made on that device.
+// once per device, with that device current, on the first call made on that device.  Its
+// first 4 bytes are the device error word of the last call, which
+// msa_noalloc_read_device_error copies out.
 #include <mutex>
 
 #include "../../include/msa.h"
@@ -57,10 +59,21 @@ extern "C" msa_status_t msa_sparse_attn_decode_noalloc(const msa_config_t* cfg, 
   void* scratch = nullptr;
   msa_status_t st = noalloc_scratch(&scratch);
   if (st != MSA_OK) return st;
-  // the error word starts at zero on every call; the partial states are written before they
-  // are read
-  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return MSA_ERR_CUDA;
+  // the error word (the array's first 4 bytes) is zeroed on the stream after validation, just
+  // before the launch, so that it reports this call alone; the partial states are written
+  // before they are read
   return msa::sparse_attn_entry(cfg, cache, batch, q, selection, out, lse, scratch, kNoAllocScratchBytes, stream,
-                                false);
+                                false, true);
+}
+
+extern "C" msa_status_t msa_noalloc_read_device_error(uint32_t* flags, void* stream) {
+  if (flags == nullptr) return MSA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  msa_status_t st = noalloc_scratch(&scratch);
+  if (st != MSA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(flags, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  return MSA_OK;
 }

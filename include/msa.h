@@ -224,11 +224,32 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
  *     with that device current); make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents: calls that can
  *     overlap on the GPU (different streams, or different host threads, on one device) race
- *     and must be serialised by the caller.  The error word is cleared at the start of each
- *     call and is not readable from outside. */
+ *     and must be serialised by the caller.
+ *   - The array's device error word (bad block-table entries, bad lengths, a wait that gave
+ *     up) is zeroed on `stream` by every call that passes validation, right before its
+ *     launch (a rejected call leaves it alone), and read back with
+ *     msa_noalloc_read_device_error. */
 msa_status_t msa_sparse_attn_decode_noalloc(const msa_config_t* cfg, const msa_cache_t* cache,
                                             const msa_batch_t* batch, const uint8_t* q, const int32_t* selection,
                                             uint16_t* out, float* lse, void* stream);
+
+/* The device error word of the no-allocation entry point's array, as the last call on this
+ * device left it (MSA_DEVERR_* bits), copied into *flags; synchronises `stream`.  Like that
+ * entry point it needs no workspace, and it shares its race: a call still running on
+ * another stream may change the word.  The pages have no counterpart to it either. */
+msa_status_t msa_noalloc_read_device_error(uint32_t* flags, void* stream);
+
+/* Test hook for the failure path of the bounded waits; not part of the decode path.
+ * Launches the streaming indexer of msa_indexer_scores (q_len x num_kv_groups <= 8; else
+ * MSA_ERR_UNSUPPORTED) with its page copies withheld and every wait capped at spin_limit
+ * polls (1 .. 2^22; msa_indexer_scores uses 2^22).  Nothing then arrives on the page ring,
+ * so each warp with pages to score gives up its first wait, sets MSA_DEVERR_TIMEOUT in the
+ * workspace error word and returns, with no copy in flight; block_scores are unspecified
+ * afterwards.  The context stays usable: the next regular call computes normally.  Same
+ * arguments and workspace as msa_indexer_scores, plus spin_limit. */
+msa_status_t msa_test_indexer_stall(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                    const uint8_t* index_q, float* block_scores, void* workspace,
+                                    size_t workspace_bytes, uint32_t spin_limit, void* stream);
 
 /* Debug helper: copies the device error word out of `workspace` into *flags (this call
  * synchronises `stream`). */
