@@ -52,11 +52,11 @@ def measured_tensor_peak():
 
 
 KERNEL_SOURCES = {
-    "indexer_half_kernel": ["indexer.cu", "msa_device.cuh", "msa_kernels.h"],
+    "indexer_half_kernel": ["indexer.cu", "indexer_tile.cuh", "msa_device.cuh", "msa_kernels.h"],
     "spec_indexer_kernel": ["spec_indexer.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "prefill_indexer_kernel": ["prefill.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "bm_attn_kernel": ["prefill_attn.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
-    "attention_kernel": ["attention.cu", "msa_device.cuh", "msa_kernels.h"],
+    "attention_kernel": ["attention.cu", "attention_tile.cuh", "msa_device.cuh", "msa_kernels.h"],
 }
 
 
@@ -169,9 +169,19 @@ def reduce_max(values, world_size: int, device=None):
     return t.tolist()
 
 
+def representative_sequences(lens, n: int):
+    """n sequences at evenly spaced quantiles of the context lengths (the (i + 1/2) / n-th
+    shortest, i < n), so that the sample's mean length tracks the workload's."""
+    import numpy as np
+    order = np.argsort(np.asarray(lens), kind="stable")
+    n = min(n, len(order))
+    return sorted(int(order[int((i + 0.5) * len(order) / n)]) for i in range(n))
+
+
 class OracleSample:
-    """The CPU oracle on a bounded sample of a workload: the first few sequences, all their
-    query tokens (the last 64 for prefill), caches quantised once before any timing."""
+    """The CPU oracle on a bounded sample of a workload: a few sequences at evenly spaced
+    quantiles of its context lengths, all their query tokens (the last 64 for prefill),
+    caches quantised once before any timing."""
 
     def __init__(self, workload_name: str, n_seqs: int, rank_seed_offset: int = 0):
         from oracle import cache as OC
@@ -179,8 +189,8 @@ class OracleSample:
 
         w = syn.WORKLOADS[workload_name]
         self.w = syn.Workload(**{**w.__dict__, "seed": w.seed + rank_seed_offset})
-        self.seqs = list(range(min(n_seqs, self.w.batch)))
         _, self.table, self.lens = syn.layout(self.w)
+        self.seqs = representative_sequences(self.lens, n_seqs)
         self.cache, _, _, _ = OC.build_cache(self.w, self.lens, self.seqs, threads=os.cpu_count() or 1)
         self.q, self.qi = OC.encode_queries(self.w, self.seqs)
         T = self.w.q_len
@@ -205,7 +215,7 @@ class OracleSample:
         """Runs whole sequences of the sample (cycling) until budget_s; (queries/s, info)."""
         t_total, rows, done = 0.0, 0, []
         k = 0
-        while t_total < budget_s or not done:
+        while t_total < budget_s or len(done) % len(self.seqs) != 0:  # whole cycles of the sample
             b = self.seqs[k % len(self.seqs)]
             t0 = time.perf_counter()
             rows += self.run_one(b)
@@ -250,6 +260,102 @@ def run_reference(args):
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure_workload(name, args, rank, dev, flush, peak, bf16_peak):
+    """One more workload through msa_decode, measured like the headline: its own seeded
+    replica, a CUDA graph of one msa_decode call replayed per step, L2 flushed between steps,
+    CUDA events on the stream, clocks sampled around the timed region; then each stage alone
+    for its kernel's roofline.  Frees its device memory before returning."""
+    import numpy as np
+    import torch
+
+    import block_sparse_attention_indexer_gb300 as msa
+    from oracle import msa as OM  # byte accounting of the oracle (host arithmetic, not the GPU path)
+    from workloads import device
+
+    w = replica_workload(name, rank)
+    t0 = time.perf_counter()
+    dw = device.upload(w)
+    setup_s = time.perf_counter() - t0
+    B, T, H = w.batch, w.q_len, w.num_heads
+    out = torch.zeros(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros(B, T, H, dtype=torch.float32, device=dev)
+    sel = torch.zeros(B, T, 4, 16, dtype=torch.int32, device=dev)
+    wsp = msa.alloc_workspace(msa.MSA_OP_DECODE, dw.cfg, dw.batch, device=dev)
+    scores = torch.empty(B, T, 4, dw.batch.max_blocks, dtype=torch.float32, device=dev)
+    ws_idx = msa.alloc_workspace(msa.MSA_OP_INDEXER_SCORES, dw.cfg, dw.batch, device=dev)
+    ws_att = msa.alloc_workspace(msa.MSA_OP_SPARSE_ATTN, dw.cfg, dw.batch, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def graphed(fn):
+        if args.no_graph:
+            return fn
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay
+
+    def timed(fn, n):
+        run = graphed(fn)
+        for _ in range(args.warmup):
+            run()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i & 0xFF)
+            a.record(stream)
+            run()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed(lambda: msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, lse, sel, wsp, None), args.steps)
+    idx_ms = timed(lambda: msa.msa_indexer_scores(dw.cfg, dw.cache, dw.batch, dw.qi, scores, ws_idx, None),
+                   args.steps)
+    sel_ms = timed(lambda: msa.msa_select_blocks(dw.cfg, dw.batch, scores, sel, None), args.steps)
+    att_ms = timed(lambda: msa.msa_sparse_attn_decode(dw.cfg, dw.cache, dw.batch, dw.q, sel, out, lse, ws_att, None),
+                   args.steps)
+    clk = clocks.stop()
+    assert msa.msa_read_device_error(wsp) == 0
+
+    sel_h = sel.cpu().numpy()
+    idx_bytes, kv_bytes = OM.decode_step_bytes(dw.lens, sel_h)
+    queries = B * T
+    step_gbs = (idx_bytes + kv_bytes) / (ms / 1e3) / 1e9
+    pos = dw.lens[:, None] - T + np.arange(T)[None, :]
+    vis = np.clip(pos[:, :, None, None] - 128 * sel_h.astype(np.int64) + 1, 0, 128) * (sel_h >= 0)
+    att_flops = 4.0 * 128 * (H // 4) * float(np.sum(vis))
+    idx_kernel = indexer_kernel_for(T, 4)
+    if idx_kernel == "prefill_indexer_kernel":
+        idx_flops = 2.0 * 128 * 4 * float(np.sum(pos + 1))
+        tf = idx_flops / (idx_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": idx_kernel, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": tf / bf16_peak, "algorithmic_flops": idx_flops}
+    else:
+        gbs = idx_bytes / (idx_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": idx_kernel, "achieved": gbs, "peak": peak, "unit": "GB/s",
+                "frac": gbs / peak, "algorithmic_bytes": idx_bytes}
+    res = {"config": {"batch": B, "q_len": T, "heads": H, "mean_ctx": float(np.mean(dw.lens)),
+                      "tokens_in_cache": int(np.sum(dw.lens))},
+           "ms_per_step": ms, "queries_per_s": queries / (ms / 1e3),
+           "step_roofline": {"bound": "hbm", "algorithmic_bytes": idx_bytes + kv_bytes, "achieved": step_gbs,
+                             "unit": "GB/s", "frac": step_gbs / peak, "frac_of_8tbs": step_gbs / 8000.0},
+           "roofline": roof,
+           "stages_ms": {"indexer": idx_ms, "select": sel_ms, "attention": att_ms,
+                         "attention_gbs": kv_bytes / (att_ms / 1e3) / 1e9, "attention_bytes": kv_bytes},
+           "attention_form": "block-major (K-to-Q CSR, tcgen05)" if T >= 64 else "query-major teams (mma.sync)",
+           "attention_tflops": att_flops / (att_ms / 1e3) / 1e12,
+           "launches_per_step": 8 if T >= 64 else 4,
+           "clocks": clk, "setup_s": round(setup_s, 1)}
+    del dw, out, lse, sel, wsp, scores, ws_idx, ws_att
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args):
@@ -409,6 +515,15 @@ def run_ours(args):
     ins_ms = timed(lambda: msa.msa_nvfp4_insert(ins_x, ins_slots, ins_data, ins_scale, 128, None), args.steps)
     ins_bytes = (ins_x.numel() * 4 + ins_slots.numel() * 8 + ins_data.numel() + ins_scale.numel())
 
+    # ---- the other workloads (same process, same L2 flush and clock sampling), each freed after
+    peak_gbs, _ = measured_peaks()
+    bf16_tf, _ = measured_tensor_peak()
+    extra = {}
+    if not args.headline_only:
+        del ins_x, ins_slots, ins_data, ins_scale, ins_perm, tok_idx
+        for name in [n for n in syn.WORKLOADS if n != w0.name]:
+            extra[name] = measure_workload(name, args, rank, dev, flush, peak_gbs, bf16_tf)
+
     # ---- aggregate over ranks (max time)
     ms_step = statistics.mean(step_ms)
     e2e_s = statistics.mean(e2e_times)
@@ -479,6 +594,7 @@ def run_ours(args):
                          "achieved": ins_bytes / (ins_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": ins_bytes / (ins_ms / 1e3) / 1e9 / peak},
         "gpu_launches": launches_per_step * args.steps,
+        "workloads": extra,
         "clocks": clk,
         "setup_s": round(setup_s, 1),
         "wall_s_timed_region": wall,
@@ -505,6 +621,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--headline-only", action="store_true", help="skip the other workloads' measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

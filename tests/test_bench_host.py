@@ -58,3 +58,16 @@ def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
     src = root / "block_sparse_attention_indexer_gb300" / "csrc" / bench.KERNEL_SOURCES[kernel][0]
     src.write_text(src.read_text() + "\n// edited\n")
     assert bench.measured_traffic(kernel, "ragged64_128k") is None
+
+
+def test_cpu_sample_tracks_the_mean_context():
+    """The CPU baseline's sample sequences sit at evenly spaced length quantiles, so their mean
+    context is within a few percent of the workload's (the first sequences need not be)."""
+    import numpy as np
+    from workloads import synthetic as syn
+    _, _, lens = syn.layout(syn.WORKLOADS["ragged64_128k"])
+    picks = bench.representative_sequences(lens, 4)
+    assert len(set(picks)) == 4
+    assert abs(np.mean(lens[picks]) / np.mean(lens) - 1) < 0.05
+    assert bench.representative_sequences(lens, 100) == sorted(range(len(lens)))
+    assert bench.representative_sequences(np.array([5, 1, 3]), 1) == [2]
