@@ -22,6 +22,8 @@ from .binding import (  # noqa: F401
     default_softmax_scale,
     msa_abi_version,
     msa_clear_device_error,
+    msa_dcp_local_candidates,
+    msa_dcp_merge,
     msa_decode,
     msa_fp8_quantize,
     msa_indexer_scores,

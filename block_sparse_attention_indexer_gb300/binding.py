@@ -61,6 +61,9 @@ _SIGS = {
     "msa_fp8_quantize": (ctypes.c_int, [_P, ctypes.c_int64, _P, _P]),
     "msa_indexer_scores": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, ctypes.c_size_t, _P]),
     "msa_select_blocks": (ctypes.c_int, [_CP, _CB, _P, _P, _P]),
+    "msa_dcp_local_candidates": (ctypes.c_int, [_CP, _CC, _CB, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P,
+                                                ctypes.c_size_t, _P]),
+    "msa_dcp_merge": (ctypes.c_int, [_CP, _CB, ctypes.c_int32, _P, _P, _P, _P]),
     "msa_sparse_attn_decode": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msa_decode": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "msa_sparse_attn_decode_noalloc": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P]),
@@ -222,6 +225,24 @@ def msa_select_blocks(cfg: Config, batch: Batch, block_scores: torch.Tensor, sel
     _check("msa_select_blocks", _lib.msa_select_blocks(
         cfg.c(), batch.c(), _ptr(block_scores, torch.float32, "block_scores"),
         _ptr(selection, torch.int32, "selection"), _stream(stream)))
+
+
+def msa_dcp_local_candidates(cfg: Config, cache: PagedCache, batch: Batch, index_q: torch.Tensor, block_lo: int,
+                             block_hi: int, block_scores: torch.Tensor, cand_scores: torch.Tensor,
+                             cand_blocks: torch.Tensor, workspace: torch.Tensor, stream=None):
+    _check("msa_dcp_local_candidates", _lib.msa_dcp_local_candidates(
+        cfg.c(), cache.c(), batch.c(), _ptr(index_q, torch.uint8, "index_q"), block_lo, block_hi,
+        _ptr(block_scores, torch.float32, "block_scores"), _ptr(cand_scores, torch.float32, "cand_scores"),
+        _ptr(cand_blocks, torch.int32, "cand_blocks"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def msa_dcp_merge(cfg: Config, batch: Batch, cand_scores: torch.Tensor, cand_blocks: torch.Tensor,
+                  selection: torch.Tensor, stream=None):
+    """cand_scores / cand_blocks: [num_shards, B, T, G, 15] (the shards' outputs stacked)."""
+    _check("msa_dcp_merge", _lib.msa_dcp_merge(
+        cfg.c(), batch.c(), int(cand_scores.shape[0]), _ptr(cand_scores, torch.float32, "cand_scores"),
+        _ptr(cand_blocks, torch.int32, "cand_blocks"), _ptr(selection, torch.int32, "selection"), _stream(stream)))
 
 
 def msa_sparse_attn_decode(cfg: Config, cache: PagedCache, batch: Batch, q: torch.Tensor, selection: torch.Tensor,

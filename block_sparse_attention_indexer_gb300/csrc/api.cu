@@ -124,6 +124,8 @@ IndexerArgs indexer_args(const msa_config_t* cfg, const msa_cache_t* cache, cons
   a.err = err;
   a.lse = cfg->score_type == MSA_SCORE_LSE ? 1 : 0;
   a.spin_limit = kDefaultSpinLimit;
+  a.block_lo = 0;
+  a.block_hi = INT32_MAX;
   return a;
 }
 
@@ -291,6 +293,49 @@ msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch
   if (block_scores == nullptr || selection == nullptr) return MSA_ERR_INVALID_ARG;
   SelectArgs a = select_args(cfg, batch, block_scores, selection);
   return cuda_status(launch_select(a, static_cast<cudaStream_t>(stream)));
+}
+
+msa_status_t msa_dcp_local_candidates(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                      const uint8_t* index_q, int32_t block_lo, int32_t block_hi, float* block_scores,
+                                      float* cand_scores, int32_t* cand_blocks, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  msa_status_t st;
+  if ((st = check_config(cfg)) != MSA_OK || (st = check_batch(batch)) != MSA_OK ||
+      (st = check_cache(cache, true, false)) != MSA_OK)
+    return st;
+  if (batch->q_len * cfg->num_kv_groups > 8 || cfg->init_blocks != 0 || cfg->local_blocks != 1)
+    return MSA_ERR_UNSUPPORTED;
+  if (block_lo < 0 || block_hi <= block_lo) return MSA_ERR_INVALID_ARG;
+  if (batch->batch == 0) return MSA_OK;
+  if (index_q == nullptr || block_scores == nullptr || cand_scores == nullptr || cand_blocks == nullptr ||
+      !aligned16(index_q))
+    return MSA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < msa_workspace_bytes(MSA_OP_INDEXER_SCORES, cfg, batch) ||
+      !aligned16(workspace))
+    return MSA_ERR_WORKSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MSA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  IndexerArgs a = indexer_args(cfg, cache, batch, index_q, block_scores, static_cast<uint32_t*>(workspace));
+  a.block_lo = block_lo;
+  a.block_hi = block_hi;
+  cudaError_t e = launch_indexer(a, sms, s);
+  if (e == cudaSuccess)
+    e = launch_dcp_local(select_args(cfg, batch, block_scores, nullptr), block_lo, block_hi, cand_scores, cand_blocks,
+                         s);
+  return cuda_status(e);
+}
+
+msa_status_t msa_dcp_merge(const msa_config_t* cfg, const msa_batch_t* batch, int32_t num_shards,
+                           const float* cand_scores, const int32_t* cand_blocks, int32_t* selection, void* stream) {
+  msa_status_t st;
+  if ((st = check_config(cfg)) != MSA_OK || (st = check_batch(batch)) != MSA_OK) return st;
+  if (cfg->init_blocks != 0 || cfg->local_blocks != 1 || num_shards < 1 || num_shards > kDcpShardsMax)
+    return MSA_ERR_UNSUPPORTED;
+  if (batch->batch == 0) return MSA_OK;
+  if (cand_scores == nullptr || cand_blocks == nullptr || selection == nullptr) return MSA_ERR_INVALID_ARG;
+  return cuda_status(launch_dcp_merge(select_args(cfg, batch, nullptr, selection), num_shards, cand_scores,
+                                      cand_blocks, static_cast<cudaStream_t>(stream)));
 }
 
 msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,

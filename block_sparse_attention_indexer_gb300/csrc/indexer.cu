@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
   const int T = a.q_len, G = a.groups;
   const int rows = T * G;  // <= 8
 
-  build_prefix(a.seq_lens, a.batch, a.q_len, a.max_blocks, a.err, prefix, warp_tot, kHWarps);
+  build_prefix(a.seq_lens, a.batch, a.q_len, a.max_blocks, a.block_lo, a.block_hi, a.err, prefix, warp_tot, kHWarps);
   if (lane == 0)
     for (int s = 0; s < kHStages; ++s) mbar_init(&bars[warp * kHStages + s], 1);
   fence_mbar_init();
@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
   auto lookup_next = [&]() {
     if (ic.u < u1) {
       ic.settle(prefix);
-      next_page = __ldg(a.block_table + static_cast<int64_t>(ic.b) * a.max_blocks + (ic.u - prefix[ic.b]));
+      next_page =
+          __ldg(a.block_table + static_cast<int64_t>(ic.b) * a.max_blocks + (a.block_lo + ic.u - prefix[ic.b]));
     }
   };
   uint32_t valid_bits = 0;
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
     cc.u = u;
     cc.settle(prefix);
     const int b = cc.b;
-    const int n = static_cast<int>(u - prefix[b]);
+    const int n = a.block_lo + static_cast<int>(u - prefix[b]);
     if (b != cur_b) {
       cur_b = b;
       L = a.seq_lens[b];
@@ -219,13 +220,15 @@ __global__ void __launch_bounds__(kHWarps * 32, 1) indexer_half_kernel(const Ind
       mbar_wait(&my_bars[k % kHStages], static_cast<uint32_t>((k / kHStages) & 1), a.spin_limit);
   }
 
-  // ---- -inf for blocks past each sequence's end (and whole rows of skipped sequences)
+  // ---- -inf for the blocks not scored: past each sequence's end, outside [block_lo, block_hi)
+  // (and whole rows of skipped sequences)
   const int64_t nrows = static_cast<int64_t>(a.batch) * rows;
   for (int64_t row = gw; row < nrows; row += nwarps) {
     const int b = static_cast<int>(row / rows);
-    const int nb = prefix[b + 1] - prefix[b];
+    const int n1 = a.block_lo + (prefix[b + 1] - prefix[b]);  // scored: [block_lo, n1)
     float* dst = a.block_scores + row * a.max_blocks;
-    for (int n = nb + lane; n < a.max_blocks; n += 32) dst[n] = -INFINITY;
+    for (int n = lane; n < a.max_blocks; n += 32)
+      if (n < a.block_lo || n >= n1) dst[n] = -INFINITY;
   }
 }
 

@@ -48,11 +48,20 @@ struct PageCursor {
   }
 };
 
-// Exclusive prefix over sequences of their work units (pages); sequences with
-// an invalid length get none (and flag MSA_DEVERR_BAD_SEQLEN once).  Block-wide scan, ends
-// with __syncthreads.  prefix has batch + 1 entries; warp_tot one entry per warp of the block.
+// Pages of a sequence of length L that a scan of logical blocks [block_lo, block_hi) reads.
+__device__ __forceinline__ int range_pages(int L, int block_lo, int block_hi) {
+  const int nb = (L + kBlock - 1) / kBlock;
+  const int hi = nb < block_hi ? nb : block_hi;
+  return hi > block_lo ? hi - block_lo : 0;
+}
+
+// Exclusive prefix over sequences of their work units (their pages among logical blocks
+// [block_lo, block_hi)); sequences with an invalid length get none (and flag
+// MSA_DEVERR_BAD_SEQLEN once).  Block-wide scan, ends with __syncthreads.  prefix has batch + 1
+// entries; warp_tot one entry per warp of the block.
 __device__ __forceinline__ void build_prefix(const int32_t* seq_lens, int batch, int q_len, int max_blocks,
-                                             uint32_t* err, int32_t* prefix, int32_t* warp_tot, int nwarps) {
+                                             int block_lo, int block_hi, uint32_t* err, int32_t* prefix,
+                                             int32_t* warp_tot, int nwarps) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = q_len;
   const int64_t cap = static_cast<int64_t>(max_blocks) * kBlock;
@@ -63,7 +72,7 @@ __device__ __forceinline__ void build_prefix(const int32_t* seq_lens, int batch,
     const int L = seq_lens[b];
     const bool ok = (L >= T) && (L <= cap);
     if (L != 0 && !ok && blockIdx.x == 0) flag_error(err, MSA_DEVERR_BAD_SEQLEN);
-    local += ok ? ((L + kBlock - 1) / kBlock) : 0;
+    local += ok ? range_pages(L, block_lo, block_hi) : 0;
   }
   int incl = local;
 #pragma unroll
@@ -80,7 +89,7 @@ __device__ __forceinline__ void build_prefix(const int32_t* seq_lens, int batch,
     prefix[b] = run;
     const int L = seq_lens[b];
     const bool ok = (L >= T) && (L <= cap);
-    run += ok ? ((L + kBlock - 1) / kBlock) : 0;
+    run += ok ? range_pages(L, block_lo, block_hi) : 0;
   }
   if (tid == blockDim.x - 1) {
     int tot = 0;

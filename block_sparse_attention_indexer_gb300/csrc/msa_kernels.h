@@ -25,6 +25,7 @@ struct IndexerArgs {
   int32_t lse;                 // block pooling: 0 max, 1 log-sum-exp
   uint32_t spin_limit;         // polls per bounded wait (streaming kernel)
   int32_t test_withhold;       // test hook: the streaming kernel issues no page copies
+  int32_t block_lo, block_hi;  // logical blocks scored (streaming kernel; others get -inf)
 };
 
 struct SelectArgs {
@@ -83,6 +84,14 @@ cudaError_t launch_spec_indexer(const IndexerArgs& a, int num_sms, cudaStream_t 
 // query rows (token x group) per sequence from which the GEMM form is used
 constexpr int kPrefillMinRows = 64;
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+// Decode context parallelism: a shard's best top_k - 1 candidates among logical blocks [lo, hi)
+// of every row ([rows][15] scores and block ids, rank order), and the owner's merge of S such
+// lists ([S][rows][15] each) into the selection.
+cudaError_t launch_dcp_local(const SelectArgs& a, int lo, int hi, float* cand_scores, int32_t* cand_blocks,
+                             cudaStream_t s);
+cudaError_t launch_dcp_merge(const SelectArgs& a, int S, const float* cand_scores, const int32_t* cand_blocks,
+                             cudaStream_t s);
+constexpr int kDcpShardsMax = 8;
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s);
 
 // KV-block-major attention for long query chunks (chunked prefill): K-to-Q CSR plan, block

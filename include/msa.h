@@ -183,6 +183,38 @@ msa_status_t msa_indexer_scores(const msa_config_t* cfg, const msa_cache_t* cach
 msa_status_t msa_select_blocks(const msa_config_t* cfg, const msa_batch_t* batch, const float* block_scores,
                                int32_t* selection, void* stream);
 
+/* Decode context parallelism, shard side ("vLLM liefert Day-0-Unterstützung für
+ * MiniMax-M3.1-Flash", §NVFP4-Indexer-DCP: each GPU scores every index-query head over its
+ * slice of the context, keeps a local top-16 per head and sends it to the head's owner, who
+ * merges exactly).  On one GPU a shard is a range of logical blocks of every sequence.
+ * Scores logical blocks [block_lo, block_hi) exactly as msa_indexer_scores does into
+ * block_scores (same layout; -inf for blocks outside the range or past the sequence end),
+ * then writes for every (b, t, g) row the shard's best top_k - 1 blocks among
+ * [block_lo, min(block_hi, r)) -- r the row's recent block, which the owner adds -- ranked
+ * as msa_select_blocks ranks (score descending, then index ascending; NaN below -inf), best
+ * first, with their scores:
+ *   cand_scores  float [batch][q_len][G][15]   cand_blocks  int32 [batch][q_len][G][15]
+ *   (-inf / -1 past the end of a shorter list).
+ * Supported: q_len x num_kv_groups <= 8 (decode) and the recipe's init_blocks == 0,
+ * local_blocks == 1, else MSA_ERR_UNSUPPORTED; 0 <= block_lo < block_hi, else
+ * MSA_ERR_INVALID_ARG.  workspace: msa_workspace_bytes(MSA_OP_INDEXER_SCORES, ...). */
+msa_status_t msa_dcp_local_candidates(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                      const uint8_t* index_q, int32_t block_lo, int32_t block_hi, float* block_scores,
+                                      float* cand_scores, int32_t* cand_blocks, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/* Decode context parallelism, owner side: merges the candidate lists of num_shards shards
+ * (1..8; disjoint block ranges that together cover every block of every sequence) into the
+ * selection: the best top_k - 1 of all candidates plus each row's recent block, ascending, -1
+ * padded to 16 (every block 0 .. r when r + 1 <= top_k).
+ *   cand_scores  float [num_shards][batch][q_len][G][15], cand_blocks int32 alike (the
+ *   shards' outputs, concatenated in any shard order).
+ * The merge is exact: top_k - 1 of the union of each shard's top_k - 1 is the global top_k - 1
+ * under one strict order, so the selection is bit-identical to msa_select_blocks on the
+ * unsharded scores.  Same support rules as the shard side; no workspace. */
+msa_status_t msa_dcp_merge(const msa_config_t* cfg, const msa_batch_t* batch, int32_t num_shards,
+                           const float* cand_scores, const int32_t* cand_blocks, int32_t* selection, void* stream);
+
 /* Stage 3 -- exact sparse GQA attention over the selected blocks.  Every head h of group g
  * attends, with logits (q . k) * softmax_scale, to the visible keys of selection[b][t][g][:];
  * K/V are dequantised exactly from NVFP4 in the kernel.  out is rounded to bfloat16;
