@@ -336,11 +336,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
 // Rows cut by team-range boundaries: combine the partial states the teams left.  One CTA per
 // boundary (the first boundary inside a row owns the row); its first warp lists the row's
 // partial slots in shared memory (arithmetic only, so it runs before the wait on the
-// attention kernel), then one thread per (head, pair of dims) makes one online pass over
-// them, so that all their loads are in flight together.
+// attention kernel), then one thread per (head, pair of dims) loads the slots' states eight
+// at a time (a row has at most 16 slots, one per selection entry) and combines them; two
+// CTAs fit an SM, so the CTAs with no row to merge clear out in one wave.
 constexpr int kMergeThreads = kHeadsMax * kDim / 2;
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a, int NT) {
+__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const AttnArgs a, int NT) {
   __shared__ int s_slot[kTopK];
   __shared__ int s_n, s_row;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -378,25 +379,42 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a, 
   const int h = tid / (kDim / 2), d = 2 * (tid % (kDim / 2));
   if (R < 0 || h >= a.heads_per_group) return;
   grid_dependency_wait();  // the attention kernel's partial states
+  // the slots' states are loaded eight at a time before any of them is used (one round of
+  // loads in flight per eight slots, not one per slot), then folded into the running sums
+  constexpr int kBatch = 8;
   float M = -INFINITY, num0 = 0.f, num1 = 0.f, den = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < n; ++i) {
-    const float* part = a.partial + static_cast<int64_t>(s_slot[i]) * kSlotFloats + h * (kDim + 2);
-    const float ms = __ldcg(part + kDim), ls = __ldcg(part + kDim + 1);
-    const float2 os = __ldcg(reinterpret_cast<const float2*>(part + d));
-    if (ms == -INFINITY) continue;
-    if (ms > M) {
-      const float f = (M == -INFINITY) ? 0.f : exp2f(M - ms);
-      num0 = num0 * f + os.x;
-      num1 = num1 * f + os.y;
-      den = den * f + ls;
-      M = ms;
-    } else {
-      const float f = exp2f(ms - M);
-      num0 += f * os.x;
-      num1 += f * os.y;
-      den += f * ls;
+  for (int i0 = 0; i0 < n; i0 += kBatch) {
+    float ms[kBatch], ls[kBatch];
+    float2 os[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      ms[i] = -INFINITY;
+      ls[i] = 0.f;
+      os[i] = make_float2(0.f, 0.f);
+      if (i0 + i < n) {
+        const float* part = a.partial + static_cast<int64_t>(s_slot[i0 + i]) * kSlotFloats + h * (kDim + 2);
+        ms[i] = __ldcg(part + kDim);
+        ls[i] = __ldcg(part + kDim + 1);
+        os[i] = __ldcg(reinterpret_cast<const float2*>(part + d));
+      }
     }
+    float Mb = M;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) Mb = fmaxf(Mb, ms[i]);
+    if (Mb == -INFINITY) continue;
+    const float fo = (M == -INFINITY) ? 0.f : exp2f(M - Mb);  // rescale the sums so far
+    num0 *= fo;
+    num1 *= fo;
+    den *= fo;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (ms[i] == -INFINITY) continue;
+      const float f = exp2f(ms[i] - Mb);
+      num0 += f * os[i].x;
+      num1 += f * os[i].y;
+      den += f * ls[i];
+    }
+    M = Mb;
   }
   const int head_row = R * a.heads_per_group + h;
   write_out(a.out, a.lse, head_row, d, num0, den, M);
