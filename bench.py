@@ -56,7 +56,7 @@ KERNEL_SOURCES = {
     "spec_indexer_kernel": ["spec_indexer.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "prefill_indexer_kernel": ["prefill.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
     "bm_attn_kernel": ["prefill_attn.cu", "msa_device.cuh", "msa_kernels.h", "umma.cuh"],
-    "attention_kernel": ["attention.cu", "attention_tile.cuh", "msa_device.cuh", "msa_kernels.h"],
+    "attention_kernel": ["attention.cu", "attention_team.cuh", "attention_tile.cuh", "msa_device.cuh", "msa_kernels.h"],
 }
 
 

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa.so")
 SOURCES = ["api.cu", "quant.cu", "indexer.cu", "prefill.cu", "select.cu", "attention.cu", "prefill_attn.cu", "spec_indexer.cu", "noalloc.cu"]
 HEADERS = ["msa_device.cuh", "msa_kernels.h", "api_internal.h", "select_row.cuh", "umma.cuh", "indexer_tile.cuh",
-           "attention_tile.cuh"]
+           "attention_tile.cuh", "attention_team.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

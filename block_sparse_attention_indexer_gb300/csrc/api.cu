@@ -242,7 +242,8 @@ size_t msa_workspace_bytes(msa_op_t op, const msa_config_t* cfg, const msa_batch
     case MSA_OP_INDEXER_SCORES: return kErrBytes;
     case MSA_OP_SELECT_BLOCKS: return 0;
     case MSA_OP_SPARSE_ATTN: return kErrBytes + attn_scratch_bytes(cfg, batch);
-    case MSA_OP_DECODE: return kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch) + attn_scratch_bytes(cfg, batch);
+    case MSA_OP_DECODE:
+      return kErrBytes + scores_bytes(cfg, batch) + 2 * sel_bytes(cfg, batch) + attn_scratch_bytes(cfg, batch);
   }
   return 0;
 }
@@ -367,11 +368,21 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
   int32_t* sel = selection_out != nullptr
                      ? selection_out
                      : reinterpret_cast<int32_t*>(ws + kErrBytes + scores_bytes(cfg, batch));
-  uint8_t* scratch = ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch);
+  int32_t* pages = reinterpret_cast<int32_t*>(ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch));
+  uint8_t* scratch = ws + kErrBytes + scores_bytes(cfg, batch) + 2 * sel_bytes(cfg, batch);
+  // the selection looks the selected pages up for the team attention kernel; the step's
+  // inputs were written before its first kernel, which waited for them
+  SelectArgs sa = select_args(cfg, batch, scores, sel);
+  sa.inputs_early = 1;
+  if (!block_major(cfg, batch)) {
+    sa.block_table = batch->block_table;
+    sa.sel_pages = pages;
+  }
   cudaError_t e = run_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
-  if (e == cudaSuccess) e = launch_select(select_args(cfg, batch, scores, sel), s);
+  if (e == cudaSuccess) e = launch_select(sa, s);
   AttnArgs aa = attn_args(cfg, cache, batch, q, sel, out, lse, reinterpret_cast<float*>(scratch), err);
   aa.q_early = 1;  // the kernel before it is this step's selection
+  if (select_writes_pages(sa)) aa.sel_pages = pages;
   if (e == cudaSuccess) e = run_attention(cfg, batch, aa, scratch, sms, s, true);
   return cuda_status(e);
 }

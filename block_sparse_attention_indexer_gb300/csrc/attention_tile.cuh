@@ -184,16 +184,19 @@ __device__ __forceinline__ void attend_quarter(const uint8_t* kd, int qk, int n,
 
 // A row's selection in two steps, so that a row's loads can be in flight while the row before
 // it is being streamed: row_fetch issues the loads that depend only on the row
-// (its selection, lane j < 16: block id of entry j, and its sequence length), row_resolve
-// then checks them and looks up the page of each entry (-1: empty, past the recent block,
-// or a bad block-table entry).
+// (its selection, lane j < 16: block id of entry j and, on the decode step, its page; the
+// sequence length), row_resolve then checks them and, unless the page came with the block
+// id, looks it up in the block table (-1: empty, past the recent block, or a bad block-table
+// entry).
 struct RowRaw {
-  int blk, L;
+  int blk, page, L;
 };
 
 __device__ __forceinline__ RowRaw row_fetch(const AttnArgs& a, int R, int lane) {
   RowRaw raw;
-  raw.blk = lane < kTopK ? a.selection[static_cast<int64_t>(R) * kTopK + lane] : -1;
+  const int64_t e = static_cast<int64_t>(R) * kTopK + lane;
+  raw.blk = lane < kTopK ? a.selection[e] : -1;
+  raw.page = (lane < kTopK && a.sel_pages != nullptr) ? a.sel_pages[e] : -1;
   raw.L = a.seq_lens[static_cast<unsigned>(R) / static_cast<unsigned>(a.q_len * a.groups)];
   return raw;
 }
@@ -209,9 +212,11 @@ __device__ __forceinline__ void row_resolve(const AttnArgs& a, int R, const RowR
   pos = L - a.q_len + t;
   const int r = ok ? pos / kBlock : -1;
   blk = ok ? raw.blk : -1;
-  // the table lookup only needs an in-range block id; its validity comes from ok and r
+  // the table lookup only needs an in-range block id; its validity comes from ok and r (the
+  // decode step's selection kernel has looked the pages up already: the same table entries)
   int p = -1;
-  if (blk >= 0 && blk < a.max_blocks) p = a.block_table[static_cast<int64_t>(b) * a.max_blocks + blk];
+  if (blk >= 0 && blk < a.max_blocks)
+    p = a.sel_pages != nullptr ? raw.page : a.block_table[static_cast<int64_t>(b) * a.max_blocks + blk];
   page = -1;
   if (blk >= 0 && blk <= r) {
     if (p >= 0 && p < a.num_pages)

@@ -35,6 +35,13 @@ struct SelectArgs {
   int32_t* selection;          // [B][T][G][16]
   int32_t top_k, init_blocks, local_blocks;
   int32_t row_cap;             // candidates per row staged in shared memory (set by the launcher)
+  // decode step only (else null / 0): the page of every selected entry, [B][T][G][16] (-1 where
+  // the selection is -1), looked up in block_table ([B][max_blocks]); inputs_early: seq_lens
+  // and block_table were written before the previous kernel on the stream started, so they
+  // may be read before waiting on it
+  const int32_t* block_table;
+  int32_t* sel_pages;
+  int32_t inputs_early;
 };
 
 struct AttnArgs {
@@ -48,6 +55,7 @@ struct AttnArgs {
   int32_t batch, max_blocks, q_len, groups, heads_per_group;
   const uint8_t* q;            // [B][T][H][128] E4M3
   const int32_t* selection;    // [B][T][G][16]
+  const int32_t* sel_pages;    // null, or the page of every selected entry (written with the selection)
   uint16_t* out;               // [B][T][H][128] bf16
   float* lse;                  // [B][T][H] or null
   float* partial;              // attn_partial_bytes(): two partial-state slots per CTA
@@ -84,6 +92,10 @@ cudaError_t launch_spec_indexer(const IndexerArgs& a, int num_sms, cudaStream_t 
 // query rows (token x group) per sequence from which the GEMM form is used
 constexpr int kPrefillMinRows = 64;
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+// whether launch_select(a) fills a.sel_pages (the CTA-per-row form, the table row staged in
+// shared memory: decode rows of at most kSelTableCap blocks)
+bool select_writes_pages(const SelectArgs& a);
+constexpr int kSelTableCap = 4096;
 // Decode context parallelism: a shard's best top_k - 1 candidates among logical blocks [lo, hi)
 // of every row ([rows][15] scores and block ids, rank order), and the owner's merge of S such
 // lists ([S][rows][15] each) into the selection.

@@ -6,14 +6,12 @@
 
 namespace msa {
 
-constexpr int kSelWarps = 4;
-constexpr int kSelCap = 512;
 constexpr int64_t kSplitMaxRows = 2048;  // rows up to which a CTA per row beats a warp per row
 
 template <int KPL>
 __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs a) {
   extern __shared__ __align__(16) uint32_t sord_all[];  // [kSelWarps][row_cap] staged score orders
-  __shared__ uint64_t buf[kSelWarps][kSelCap];
+  __shared__ __align__(16) uint64_t buf[kSelWarps][kSelCap];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // launched as a programmatic dependent of the previous kernel on the stream: wait for it
   // (and its memory) before touching global memory
@@ -43,73 +41,39 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs
 // at most NW x 16 keys); the first warp ranks those exact keys against each other -- each
 // lane holds NW / 2 of them and compares them with every key by shuffles -- and each of the
 // W winners writes its block id at its rank, then a warp sort puts them in ascending order.
+//
+// On the decode step (a.sel_pages set) the CTA also stages its sequence's block-table row in
+// shared memory and writes the page of every selected block, so that the attention kernel
+// reads each entry's page with its block id instead of looking it up after reading the
+// selection; with a.inputs_early the sequence length and the table row are read before the
+// wait on the indexer, while its last CTAs are still running.
 template <int NW, int KPL>
 __global__ void __launch_bounds__(NW * 32) select_split_kernel(const SelectArgs a) {
-  constexpr int kKeys = NW * kTopK / 32;  // candidate keys per lane in the final ranking
-  __shared__ uint64_t buf[NW][kSelCap / 8];
-  __shared__ int32_t part[NW][kTopK];
-  __shared__ int32_t win_ids[kTopK];
+  __shared__ __align__(16) uint64_t buf[NW][kSelCap / 8];
+  __shared__ __align__(16) uint64_t part[NW][kTopK];
+  __shared__ __align__(16) int32_t win_ids[kTopK];
+  extern __shared__ int32_t tab[];  // [max_blocks] when pages are written
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  grid_dependency_wait();
-  grid_dependents_launch();
   const int64_t row = blockIdx.x;
   const int b = static_cast<int>(row / (static_cast<int64_t>(a.q_len) * a.groups));
-  const int t = static_cast<int>((row / a.groups) % a.q_len);
-  int32_t* out = a.selection + row * kTopK;
-  const int L = a.seq_lens[b];
-  if (L < a.q_len || L <= 0 || L > static_cast<int64_t>(a.max_blocks) * kBlock) {
-    if (warp == 0 && lane < kTopK) out[lane] = -1;
-    return;
+  const bool stage_tab = a.sel_pages != nullptr;
+  const int32_t* tab_src = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+  int L = 0;
+  if (a.inputs_early) {
+    L = a.seq_lens[b];
+    if (stage_tab)
+      for (int i = threadIdx.x; i < a.max_blocks; i += NW * 32) tab[i] = __ldg(tab_src + i);
   }
-  const int r = (L - a.q_len + t) / kBlock;
-  if (r + 1 <= a.top_k) {  // every block 0 .. r
-    if (warp == 0 && lane < kTopK) out[lane] = lane <= r ? lane : -1;
-    return;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  if (!a.inputs_early) {
+    L = a.seq_lens[b];
+    if (stage_tab)
+      for (int i = threadIdx.x; i < a.max_blocks; i += NW * 32) tab[i] = __ldg(tab_src + i);
   }
-  const float* sc = a.block_scores + row * a.max_blocks;
-  const int lo = a.init_blocks, hi = r - a.local_blocks + 1, W = a.top_k - a.init_blocks - a.local_blocks;
-  const int span = (hi - lo + NW - 1) / NW;
-  const int wlo = min(hi, lo + warp * span), whi = min(hi, wlo + span);
-  const int ww = min(W, whi - wlo);
-  const int id = top_blocks_warp<KPL>(sc, wlo, whi, ww, lane, nullptr, 0, buf[warp], kSelCap / 8);
-  if (lane < kTopK) part[warp][lane] = id;
-  __syncthreads();
-  if (warp != 0) return;
-  // exact keys of the shares' winners (0: empty slot, below every key)
-  uint64_t key[kKeys];
-#pragma unroll
-  for (int i = 0; i < kKeys; ++i) {
-    const int n = (&part[0][0])[32 * i + lane];
-    key[i] = n >= 0 ? (static_cast<uint64_t>(score_order(__ldcg(sc + n))) << 32) |
-                          static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(n))
-                    : 0ull;
-  }
-  // rank of each key = keys larger than it (all keys distinct)
-  int rank[kKeys];
-#pragma unroll
-  for (int i = 0; i < kKeys; ++i) rank[i] = 0;
-#pragma unroll
-  for (int i2 = 0; i2 < kKeys; ++i2)
-#pragma unroll 4
-    for (int j = 0; j < 32; ++j) {
-      const uint64_t other = shfl_u64(key[i2], j);
-#pragma unroll
-      for (int i = 0; i < kKeys; ++i) rank[i] += other > key[i] ? 1 : 0;
-    }
-#pragma unroll
-  for (int i = 0; i < kKeys; ++i)
-    if (key[i] != 0ull && rank[i] < W) win_ids[rank[i]] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key[i]));
-  __syncwarp();
-  const int sorted_id = warp_sort_asc_i32(lane < W ? win_ids[lane] : 0x7fffffff, lane);
-  const int from_win = __shfl_sync(0xffffffffu, sorted_id, (lane - a.init_blocks) & 31);
-  int v = -1;
-  if (lane < a.init_blocks)
-    v = lane;
-  else if (lane < a.init_blocks + W)
-    v = from_win;
-  else if (lane < a.top_k)
-    v = r - a.local_blocks + 1 + (lane - a.init_blocks - W);
-  if (lane < kTopK) out[lane] = v;
+  if (stage_tab) __syncthreads();
+  select_split_row<NW, KPL>(a, row, L, warp, lane, buf, part, win_ids, stage_tab ? tab : nullptr,
+                            [] { __syncthreads(); });
 }
 
 // ------------------------------------------------------------------------------------------
@@ -125,7 +89,7 @@ __global__ void __launch_bounds__(NW * 32) select_split_kernel(const SelectArgs 
 template <int KPL>
 __global__ void __launch_bounds__(kSelWarps * 32) dcp_local_kernel(const SelectArgs a, int lo, int hi,
                                                                    float* cand_scores, int32_t* cand_blocks) {
-  __shared__ uint64_t buf[kSelWarps][kSelCap / 8];
+  __shared__ __align__(16) uint64_t buf[kSelWarps][kSelCap / 8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();
   grid_dependents_launch();
@@ -259,16 +223,30 @@ cudaError_t launch_dcp_merge(const SelectArgs& a, int S, const float* cand_score
   return cudaGetLastError();
 }
 
+namespace {
+// long rows, or few rows (decode): a CTA per row; many rows (chunked prefill): a warp per row
+bool cta_per_row(const SelectArgs& a) {
+  const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
+  return a.max_blocks > 32 * 32 || nrows <= kSplitMaxRows;
+}
+}  // namespace
+
+bool select_writes_pages(const SelectArgs& a) {
+  return a.sel_pages != nullptr && a.block_table != nullptr && cta_per_row(a) && a.max_blocks <= kSelTableCap;
+}
+
 cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
   SelectArgs a = a0;
   const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.groups;
   if (nrows == 0) return cudaSuccess;
-  // long rows, or few rows (decode): a CTA per row; many rows (chunked prefill): a warp per row
+  if (!select_writes_pages(a)) a.sel_pages = nullptr;
   const bool long_rows = a.max_blocks > 32 * 32;
-  if (long_rows || nrows <= kSplitMaxRows) {
+  if (cta_per_row(a)) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(nrows));
     cfg.blockDim = dim3((long_rows ? 8 : 4) * 32);
+    // the staged table row: at most kSelTableCap entries (16 KB), under the default limit
+    cfg.dynamicSmemBytes = a.sel_pages != nullptr ? static_cast<size_t>(a.max_blocks) * sizeof(int32_t) : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -18,16 +18,24 @@
 //   2. the candidates at or above that bound (at least W, about 20 for W = 15 and the
 //      workloads' score distributions) are compacted to shared memory as their exact
 //      64-bit keys: per-lane counts, a warp prefix sum, and every lane writes its own;
-//   3. if at most 32 survive (the usual case) each survivor's rank comes from 32 pairwise
-//      comparisons across the warp, and each winner takes its place in ascending block
-//      order; otherwise W rounds of warp arg-max pick the winners, over the compacted
-//      survivors or, if they overflowed the buffer (adversarial score layouts), over all
-//      candidates, and a bitonic sort orders them.
+//   3. if at most 32 survive (the usual case) each survivor's rank is the number of survivor
+//      keys above its own, and each winner takes its place in ascending block order, the
+//      number of winners with a smaller block id; otherwise W rounds of warp arg-max pick the
+//      winners, over the compacted survivors or, if they overflowed the buffer (adversarial
+//      score layouts), over all candidates, and a bitonic sort orders them.
+// The counts in 1 and 3 read the values they compare against back from shared memory as
+// broadcast vector loads, which issue back to back; a chain of warp shuffles (a sorting
+// network, or one shuffle per compared key) waits on each shuffle's latency in turn and cost
+// this step several times as much.
 #pragma once
 
 #include "msa_device.cuh"
+#include "msa_kernels.h"
 
 namespace msa {
+
+constexpr int kSelWarps = 4;   // warps per CTA of the warp-per-row selection kernels
+constexpr int kSelCap = 512;   // survivor keys per warp there (a CTA per row keeps kSelCap / 8)
 
 __device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
   uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v), src);
@@ -95,17 +103,21 @@ __device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v, int lane) {
   return v;
 }
 
-// The W best of the candidate blocks lo .. hi-1 of one row (0 <= W <= 16, W < hi - lo):
-// returns, in lane i < W, the i-th winner in ascending block order (-1 in the other lanes).
-// s: the row's block scores (global); sord: optional shared staging of row_cap score orders
-// for more than 1,024 candidates (else they are re-read from L2); cb: a shared buffer of
+// A winner record: block id << 32 | score order (kNoWinner: none; sorts after every record).
+constexpr uint64_t kNoWinner = ~0ull;
+
+// The W best of the candidate blocks lo .. hi-1 of one row (0 <= W <= 16, W <= hi - lo):
+// returns, in lane i < W, the record of the i-th winner in ascending block order (kOrdered)
+// or in rank order, best first (kNoWinner in the other lanes).  s: the row's block scores
+// (global); sord: optional shared staging of row_cap score orders for more than 1,024
+// candidates (else they are re-read from L2); cb: a 16-byte aligned shared buffer of
 // cap >= 32 survivor keys.  All 32 lanes call it together.
 // KPL: candidates per lane held in registers (rows of up to 32 * KPL candidates); fewer
 // registers for short rows let more warps share an SM.
-template <int KPL = 32>
-__device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, int W, int lane, uint32_t* sord,
-                                               int row_cap, uint64_t* cb, int cap) {
-  if (W <= 0) return -1;
+template <int KPL = 32, bool kOrdered = true>
+__device__ __forceinline__ uint64_t top_winners_warp(const float* s, int lo, int hi, int W, int lane, uint32_t* sord,
+                                                     int row_cap, uint64_t* cb, int cap) {
+  if (W <= 0) return kNoWinner;
   const int nc = hi - lo;                 // candidates
   const bool in_regs = nc <= 32 * KPL;    // candidate orders held in registers
   const bool staged = !in_regs && sord != nullptr && nc <= row_cap;
@@ -145,8 +157,21 @@ __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, i
       }
     }
   }
-  const uint32_t bound = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lmax, lane), W - 1);
+  // the W-th largest lane maximum: held by a lane with fewer than W maxima above its own and
+  // at least W at or above it (the maxima read back from shared memory four at a time)
+  uint32_t* lm = reinterpret_cast<uint32_t*>(cb);
+  lm[lane] = lmax;
   __syncwarp();
+  int gt = 0, ge = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 x = reinterpret_cast<const uint4*>(lm)[j];
+    gt += (x.x > lmax ? 1 : 0) + (x.y > lmax ? 1 : 0) + (x.z > lmax ? 1 : 0) + (x.w > lmax ? 1 : 0);
+    ge += (x.x >= lmax ? 1 : 0) + (x.y >= lmax ? 1 : 0) + (x.z >= lmax ? 1 : 0) + (x.w >= lmax ? 1 : 0);
+  }
+  const unsigned at_w = __ballot_sync(0xffffffffu, gt < W && ge >= W);
+  const uint32_t bound = __shfl_sync(0xffffffffu, lmax, __ffs(at_w) - 1);
+  __syncwarp();  // every lane has read the maxima: the buffer takes the survivors
   auto order_of = [&](int c) -> uint32_t { return staged ? sord[c] : score_order(__ldcg(s + lo + c)); };
   auto key_of = [](uint32_t ord, int n) -> uint64_t {
     return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(n));
@@ -183,34 +208,41 @@ __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, i
       }
     }
   }
+  if (count <= 32 && lane >= count) cb[lane] = 0ull;  // below every key
   __syncwarp();
 
   // 3. the W winners in ascending block order
   if (count <= 32) {
-    // rank of each survivor by key (keys are distinct; empty lanes hold 0, below every key),
-    // then each winner's position among the winners by block index
-    const uint64_t k = lane < count ? cb[lane] : 0ull;
+    // rank of each survivor = survivor keys above its own (keys are distinct; the padding
+    // zeros are below every key), read two at a time
+    const uint64_t k = cb[lane];
     int rank = 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) rank += shfl_u64(k, j) > k ? 1 : 0;
-    const bool win = lane < count && rank < W;
-    const int id = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k));
-    const uint32_t wm = __ballot_sync(0xffffffffu, win);
+    for (int j = 0; j < 16; ++j) {
+      const ulonglong2 x = reinterpret_cast<const ulonglong2*>(cb)[j];
+      rank += (x.x > k ? 1 : 0) + (x.y > k ? 1 : 0);
+    }
+    __syncwarp();  // every survivor key is read: the buffer now takes the records, by rank
+    if (lane < count && rank < W)
+      cb[rank] = (static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(k)) << 32) | (k >> 32);
+    __syncwarp();
+    const uint64_t rec = lane < W ? cb[lane] : kNoWinner;
+    if (!kOrdered) {
+      __syncwarp();
+      return rec;
+    }
+    // place of each winner in ascending block order = winners with a smaller block id
     int at = 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int idj = __shfl_sync(0xffffffffu, id, j);
-      at += (((wm >> j) & 1u) && idj < id) ? 1 : 0;
-    }
-    __syncwarp();  // every survivor key is read: the buffer now takes the ids
-    int* ids = reinterpret_cast<int*>(cb);
-    if (win) ids[at] = id;
+    for (int j = 0; j < kTopK; ++j) at += (j < W && cb[j] < rec) ? 1 : 0;
     __syncwarp();
-    const int out = lane < W ? ids[lane] : -1;
+    if (lane < W) cb[at] = rec;
+    __syncwarp();
+    const uint64_t out = lane < W ? cb[lane] : kNoWinner;
     __syncwarp();
     return out;
   }
-  int mine = 0x7fffffff;  // lane i (< W) holds the block of the i-th winner by rank
+  uint64_t mine = kNoWinner;  // lane i (< W) holds the record of the i-th winner by rank
   {
     const bool overflow = count > cap;
     uint64_t prev = ~0ull;
@@ -236,12 +268,22 @@ __device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, i
       }
       best = warp_max_u64(best);
       prev = best;
-      if (lane == round) mine = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best));
+      if (lane == round)
+        mine = (static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(best)) << 32) | (best >> 32);
     }
   }
-  // 4. ascending order of the W ids (the other lanes carry INT_MAX)
-  const int sorted_id = warp_sort_asc_i32(mine, lane);
-  return lane < W ? sorted_id : -1;
+  if (!kOrdered) return mine;
+  // 4. ascending block order of the W records (the other lanes carry kNoWinner, sorted last)
+  const uint64_t sorted = ~warp_sort_desc_u64(~mine, lane);
+  return lane < W ? sorted : kNoWinner;
+}
+
+// The same, as block ids (-1 in the lanes past W).
+template <int KPL = 32>
+__device__ __forceinline__ int top_blocks_warp(const float* s, int lo, int hi, int W, int lane, uint32_t* sord,
+                                               int row_cap, uint64_t* cb, int cap) {
+  const uint64_t w = top_winners_warp<KPL>(s, lo, hi, W, lane, sord, row_cap, cb, cap);
+  return w == kNoWinner ? -1 : static_cast<int>(w >> 32);
 }
 
 // The selection of one row whose recent block is r: min(top_k, r + 1) blocks in ascending
@@ -263,6 +305,92 @@ __device__ __forceinline__ int select_row_warp(const float* s, int r, int top_k,
   if (lane < init_blocks + W) return from_win;
   if (lane < top_k) return r - local_blocks + 1 + (lane - init_blocks - W);
   return -1;
+}
+
+// The selection of one row by NW warps (all of them call it, with the same row and the row's
+// sequence length L, read by the caller): each warp takes the best of a contiguous share of the
+// candidates, then the first warp ranks the shares' winners by the exact keys they left in
+// shared memory.  sync() is a barrier over the NW warps; buf / part / win_ids are their shared
+// scratch (buf[NW][kSelCap / 8], part[NW][16], win_ids[16]).  If a.sel_pages is set the page of
+// every selected block is written beside it, from tab (the sequence's block-table row in shared
+// memory) or, if tab is null, from a.block_table.
+template <int NW, int KPL, typename Sync>
+__device__ __forceinline__ void select_split_row(const SelectArgs& a, int64_t row, int L, int warp, int lane,
+                                                 uint64_t (*buf)[kSelCap / 8], uint64_t (*part)[kTopK],
+                                                 int32_t* win_ids, const int32_t* tab, Sync sync) {
+  constexpr int kKeys = NW * kTopK / 32;  // candidate keys per lane in the final ranking
+  const int b = static_cast<int>(row / (static_cast<int64_t>(a.q_len) * a.groups));
+  const int t = static_cast<int>((row / a.groups) % a.q_len);
+  int32_t* out = a.selection + row * kTopK;
+  auto page_of = [&](int id) -> int32_t {
+    if (id < 0) return -1;
+    return tab != nullptr ? tab[id] : a.block_table[static_cast<int64_t>(b) * a.max_blocks + id];
+  };
+  if (L < a.q_len || L <= 0 || L > static_cast<int64_t>(a.max_blocks) * kBlock) {
+    if (warp == 0 && lane < kTopK) {
+      out[lane] = -1;
+      if (a.sel_pages != nullptr) a.sel_pages[row * kTopK + lane] = -1;
+    }
+    return;
+  }
+  const int r = (L - a.q_len + t) / kBlock;
+  if (r + 1 <= a.top_k) {  // every block 0 .. r
+    if (warp == 0 && lane < kTopK) {
+      const int v = lane <= r ? lane : -1;
+      out[lane] = v;
+      if (a.sel_pages != nullptr) a.sel_pages[row * kTopK + lane] = page_of(v);
+    }
+    return;
+  }
+  const float* sc = a.block_scores + row * a.max_blocks;
+  const int lo = a.init_blocks, hi = r - a.local_blocks + 1, W = a.top_k - a.init_blocks - a.local_blocks;
+  const int span = (hi - lo + NW - 1) / NW;
+  const int wlo = min(hi, lo + warp * span), whi = min(hi, wlo + span);
+  const int ww = min(W, whi - wlo);
+  const uint64_t rec = top_winners_warp<KPL, false>(sc, wlo, whi, ww, lane, nullptr, 0, buf[warp], kSelCap / 8);
+  // the share's winner as its exact rank key order(score) << 32 | ~id (0: none, below every key)
+  if (lane < kTopK)
+    part[warp][lane] = rec == kNoWinner ? 0ull
+                                        : (rec << 32) | static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(rec >> 32));
+  sync();
+  if (warp != 0) return;
+  uint64_t key[kKeys];
+#pragma unroll
+  for (int i = 0; i < kKeys; ++i) key[i] = (&part[0][0])[32 * i + lane];
+  // rank of each key = keys larger than it (all keys distinct), the keys read two at a time
+  int rank[kKeys];
+#pragma unroll
+  for (int i = 0; i < kKeys; ++i) rank[i] = 0;
+#pragma unroll
+  for (int j = 0; j < NW * kTopK / 2; ++j) {
+    const ulonglong2 x = reinterpret_cast<const ulonglong2*>(&part[0][0])[j];
+#pragma unroll
+    for (int i = 0; i < kKeys; ++i) rank[i] += (x.x > key[i] ? 1 : 0) + (x.y > key[i] ? 1 : 0);
+  }
+#pragma unroll
+  for (int i = 0; i < kKeys; ++i)
+    if (key[i] != 0ull && rank[i] < W) win_ids[rank[i]] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key[i]));
+  __syncwarp();
+  // ascending order: each winner's place = winners with a smaller block id
+  const int my_id = lane < W ? win_ids[lane] : 0x7fffffff;
+  int at = 0;
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) at += (j < W && win_ids[j] < my_id) ? 1 : 0;
+  __syncwarp();
+  if (lane < W) win_ids[at] = my_id;
+  __syncwarp();
+  const int from_win = win_ids[(lane - a.init_blocks) & (kTopK - 1)];
+  int v = -1;
+  if (lane < a.init_blocks)
+    v = lane;
+  else if (lane < a.init_blocks + W)
+    v = from_win;
+  else if (lane < a.top_k)
+    v = r - a.local_blocks + 1 + (lane - a.init_blocks - W);
+  if (lane < kTopK) {
+    out[lane] = v;
+    if (a.sel_pages != nullptr) a.sel_pages[row * kTopK + lane] = page_of(v);
+  }
 }
 
 }  // namespace msa

@@ -233,9 +233,13 @@ msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* 
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Fused decode step = stage 1 + stage 2 + stage 3 on one stream, intermediate scores and
- * selections kept in the workspace.  selection_out (may be NULL) receives a copy of the
- * selection.  workspace: msa_workspace_bytes(MSA_OP_DECODE, ...) (the stage-3 form follows
- * the same 64-token rule as msa_sparse_attn_decode). */
+ * selections kept in the workspace.  selection_out (may be NULL) receives the selection.
+ * workspace: msa_workspace_bytes(MSA_OP_DECODE, ...): the error word, the block scores, the
+ * selection, the page of every selected entry (looked up by the selection kernel for the
+ * team attention kernel) and the stage-3 scratch (the stage-3 form follows the same 64-token
+ * rule as msa_sparse_attn_decode).  seq_lens and block_table are read from the selection
+ * kernel's start, before the indexer has finished: like q and index_q, they must be written
+ * before the call's first kernel runs (any earlier stream-ordered write is). */
 msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                         const uint8_t* q, const uint8_t* index_q, uint16_t* out, float* lse,
                         int32_t* selection_out, void* workspace, size_t workspace_bytes, void* stream);

@@ -65,7 +65,8 @@ def test_workspace_sizes(lib):
     assert f(b.MSA_OP_INDEXER_SCORES, ctypes.byref(cfg), ctypes.byref(bt)) == 256
     assert f(b.MSA_OP_SELECT_BLOCKS, ctypes.byref(cfg), ctypes.byref(bt)) == 0
     assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + partial
-    assert f(b.MSA_OP_DECODE, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + scores + sel + partial
+    # the decode step keeps the scores, the selection and the selected entries' pages
+    assert f(b.MSA_OP_DECODE, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + scores + 2 * sel + partial
     bt = b._Batch(1, 1, 1, 544, 63)   # 63 query tokens: still the team kernel
     assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + partial
 
@@ -85,7 +86,7 @@ def test_workspace_sizes(lib):
     assert bm == 8960 + 2 * 8704 + 1048576 + 16777216 + 536870912 + 33554432
     assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + bm
     assert f(b.MSA_OP_DECODE, ctypes.byref(cfg), ctypes.byref(bt)) == (
-        256 + al(4096 * 4 * 544 * 4) + al(4096 * 4 * 16 * 4) + bm)
+        256 + al(4096 * 4 * 544 * 4) + 2 * al(4096 * 4 * 16 * 4) + bm)
     bt = b._Batch(1, 1, 2, 300, 64)
     assert f(b.MSA_OP_SPARSE_ATTN, ctypes.byref(cfg), ctypes.byref(bt)) == 256 + block_major(2, 64, 4, 8, 300)
     # unsupported configurations report 0
