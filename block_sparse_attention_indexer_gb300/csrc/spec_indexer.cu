@@ -8,15 +8,16 @@
 // [128 keys x 128] . [128 x 32 rows]: too narrow for the query rows as M, so the keys are M and
 // the rows are N (= rows rounded up to 16):
 //   * a CTA owns one sequence and a range of key blocks (sized at launch so that the grid is
-//     one round of two CTAs per SM); warp 8 streams the raw NVFP4 pages (3 stages): the E2M1
+//     one round of two CTAs per SM); warp 8 streams the raw NVFP4 pages (6 stages): the E2M1
 //     rows with a 2-D tensor copy that lands them 64-byte swizzled, the scales with a bulk
 //     copy; warps 4-7 dequantise each page exactly, one key row per thread, in registers (cvt
-//     e2m1x2 -> f16x2 times the f16 scale; the swizzle makes the eight lanes of a shared-memory
-//     phase read eight different bank groups) and store the row with tcgen05.st straight into
-//     tensor memory as the MMA's A operand (2 stages: no shared-memory round trip for the
-//     keys); warps 0-3 convert the sequence's query rows once (FP8 -> f16, the B operand in
-//     shared memory), and one thread of warp 9 issues tcgen05.mma (A from TMEM: M 128 keys x N
-//     rows x K 16, eight per page) into one of two TMEM accumulators;
+//     e2m1x2 -> f16x2 times the f16 scale, the row's eight scales converted once; the swizzle
+//     makes the eight lanes of a shared-memory phase read eight different bank groups) and
+//     store the row with tcgen05.st straight into tensor memory as the MMA's A operand (2
+//     stages: no shared-memory round trip for the keys); warps 0-3 convert the sequence's query
+//     rows once (FP8 -> f16, the B operand in shared memory), and one thread of warp 9 issues
+//     tcgen05.mma (A from TMEM: M 128 keys x N rows x K 16, eight per page) into one of two
+//     TMEM accumulators;
 //   * the epilogue warps (TMEM lane quarter = warp) load their 32 keys' scores 16 rows at a
 //     time; the causal mask is applied only on pages holding a key some row must not see.
 //     Max pooling reduces each row over the warp's keys with one warp-wide f32 max
@@ -25,7 +26,7 @@
 //     each other.  Log-sum-exp pooling reduces with a butterfly that transposes as it goes
 //     (31 shuffles leave lane c with row c over the warp's keys), sums e^{s - max} the same
 //     way and combines through shared memory;
-//   * 10 warps, ~66 KB of shared memory and 256 TMEM columns: two CTAs share an SM.
+//   * 10 warps, ~94 KB of shared memory and 256 TMEM columns: two CTAs share an SM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -39,7 +40,7 @@
 namespace msa {
 
 constexpr int kSpKbMax = 64;       // key blocks per CTA at most (the launch sizes the ranges)
-constexpr int kSpRawSt = 3;        // raw page stages (shared memory)
+constexpr int kSpRawSt = 6;        // raw page stages (shared memory)
 constexpr int kSpSt = 2;           // f16 key stages (TMEM, 64 columns each)
 constexpr int kSpDeqWarps = 4;     // dequantisers (warps 4-7)
 constexpr int kSpCopyWarp = 8, kSpMmaWarp = 9;
@@ -238,6 +239,9 @@ __global__ void __launch_bounds__(kSpWarps * 32, 2) spec_indexer_kernel(const In
         tc_fence_after();
         const uint8_t* src = raw + rs * kSpRaw;
         const uint2 scw = lds64(src + kPageData + key * kRowScales);  // the row's 8 scales
+        uint32_t sc[8];  // each as an f16 pair (s, s), converted once per row
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc[i] = e4m3_bcast_f16x2(i < 4 ? scw.x : scw.y, i & 3);
         // register r = dims 2r, 2r+1 (f16 pair): the row laid along its TMEM lane's columns
         uint32_t hv[64];
 #pragma unroll
@@ -248,14 +252,13 @@ __global__ void __launch_bounds__(kSpWarps * 32, 2) spec_indexer_kernel(const In
           const uint32_t wd[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {  // 8 dims 32c + 8i .. +7: scale 2c + i / 2
-            const int si = 2 * c + (i >> 1);
-            const uint32_t sc = e4m3_bcast_f16x2(si < 4 ? scw.x : scw.y, si & 3);
+            const uint32_t f = sc[2 * c + (i >> 1)];
             uint32_t x0, x1, x2, x3;
             e2m1x8_to_f16x2(wd[i], x0, x1, x2, x3);
-            hv[16 * c + 4 * i] = hmul2(x0, sc);
-            hv[16 * c + 4 * i + 1] = hmul2(x1, sc);
-            hv[16 * c + 4 * i + 2] = hmul2(x2, sc);
-            hv[16 * c + 4 * i + 3] = hmul2(x3, sc);
+            hv[16 * c + 4 * i] = hmul2(x0, f);
+            hv[16 * c + 4 * i + 1] = hmul2(x1, f);
+            hv[16 * c + 4 * i + 2] = hmul2(x2, f);
+            hv[16 * c + 4 * i + 3] = hmul2(x3, f);
           }
         }
         tmem_st64(trow + s * kSpACols, hv);
