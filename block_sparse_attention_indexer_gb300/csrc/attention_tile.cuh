@@ -1,5 +1,5 @@
-// Device building blocks of the exact sparse GQA attention over NVFP4 K/V pages, shared by the
-// query-major team kernel (attention.cu) and the fused decode step (decode_fused.cu).
+// Device building blocks of the exact sparse GQA attention over NVFP4 K/V pages, used by the
+// query-major team kernel (attention_team.cuh, attention.cu).
 //
 // Every query head of a KV group attends exactly to the selected blocks of that group
 // ("vLLM liefert Day-0-Unterstützung für MiniMax-M3.1-Flash", §MSA-Grundlagen, Fig. 1), with

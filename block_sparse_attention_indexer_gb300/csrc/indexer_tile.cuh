@@ -1,6 +1,6 @@
-// Device building blocks of the index-key scan shared by the streaming indexer
-// (indexer.cu) and the fused decode step (decode_fused.cu): the flattened (sequence, page)
-// unit list and the exact NVFP4 x FP8 score tile on mma.sync.
+// Device building blocks of the streaming index-key scan (indexer.cu): the flattened
+// (sequence, page) unit list, the exact NVFP4 x FP8 score tile on mma.sync and one CTA's share
+// of the scan.
 //
 // Scores are the plain dot products of one index query per (query token, KV group) with every
 // cached index key ("vLLM liefert Day-0-Unterstützung für MiniMax-M3.1-Flash",
