@@ -336,11 +336,11 @@ def measure_workload(name, args, rank, dev, flush, peak, bf16_peak):
         idx_flops = 2.0 * 128 * 4 * float(np.sum(pos + 1))
         tf = idx_flops / (idx_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": idx_kernel, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": tf / bf16_peak, "algorithmic_flops": idx_flops}
+                "frac": tf / bf16_peak, "algorithmic_flops": idx_flops, "traffic": measured_traffic(idx_kernel, name)}
     else:
         gbs = idx_bytes / (idx_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": idx_kernel, "achieved": gbs, "peak": peak, "unit": "GB/s",
-                "frac": gbs / peak, "algorithmic_bytes": idx_bytes}
+                "frac": gbs / peak, "algorithmic_bytes": idx_bytes, "traffic": measured_traffic(idx_kernel, name)}
     res = {"config": {"batch": B, "q_len": T, "heads": H, "mean_ctx": float(np.mean(dw.lens)),
                       "tokens_in_cache": int(np.sum(dw.lens))},
            "ms_per_step": ms, "queries_per_s": queries / (ms / 1e3),
