@@ -171,3 +171,54 @@ def test_host_validation_rejects_before_launch():
     q_mis = buf[1:1 + dw.q.numel()].view(dw.q.shape)
     with pytest.raises(msa.MsaError, match="INVALID_ARG"):
         msa.msa_decode(dw.cfg, dw.cache, dw.batch, q_mis, dw.qi, out, None, None, ws)
+
+
+def test_inputs_written_by_the_kernel_just_before_are_seen():
+    """On the decode step the selection reads seq_lens and the block table before its wait on
+    the indexer (the step's inputs were written before its first kernel, which waits for the
+    writer).  Inputs written by kernels queued on the same stream right before msa_decode,
+    with no synchronisation, must give bit-for-bit the result of the same inputs written
+    beforehand; the old inputs give a different one."""
+    need_gpu()
+    import torch
+    import block_sparse_attention_indexer_gb300 as msa
+    lens = [20000, 9000, 3000, 129, 40000, 5000, 16 * 128 + 5, 700]
+    w, lens = syn.custom("inputs_early", 131, len(lens), 1, 8, lens, shuffled=True)
+    dw = device_workload(w, lens)
+    B, T, H = w.batch, w.q_len, w.num_heads
+    old_table, old_lens = dw.batch.block_table.clone(), dw.batch.seq_lens.clone()
+    # new inputs: sequence b takes sequence b - 1's length and pages
+    new_table, new_lens = torch.roll(old_table, 1, 0).contiguous(), torch.roll(old_lens, 1, 0).contiguous()
+
+    def decode(batch):
+        out = torch.zeros(B, T, H, 128, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros(B, T, H, dtype=torch.float32, device="cuda")
+        sel = torch.full((B, T, 4, 16), 7, dtype=torch.int32, device="cuda")
+        ws = msa.alloc_workspace(msa.MSA_OP_DECODE, dw.cfg, batch)
+        torch.cuda.synchronize()
+        return out, lse, sel, ws
+
+    # reference: the new inputs in place before the call
+    ref_b = msa.Batch(new_table.clone(), new_lens.clone(), 1)
+    o_ref, l_ref, s_ref, ws = decode(ref_b)
+    msa.msa_decode(dw.cfg, dw.cache, ref_b, dw.q, dw.qi, o_ref, l_ref, s_ref, ws)
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_error(ws) == 0
+    # the same call with the old inputs
+    old_b = msa.Batch(old_table.clone(), old_lens.clone(), 1)
+    o_old, l_old, s_old, ws_old = decode(old_b)
+    msa.msa_decode(dw.cfg, dw.cache, old_b, dw.q, dw.qi, o_old, l_old, s_old, ws_old)
+    torch.cuda.synchronize()
+    assert not torch.equal(s_old, s_ref)
+    # the buffers hold the old inputs; elementwise kernels write the new ones on the stream,
+    # and msa_decode follows them with no synchronisation in between
+    for _ in range(3):
+        t_b = msa.Batch(old_table.clone(), old_lens.clone(), 1)
+        o, l, s, ws_t = decode(t_b)
+        torch.add(new_table, 0, out=t_b.block_table)
+        torch.add(new_lens, 0, out=t_b.seq_lens)
+        msa.msa_decode(dw.cfg, dw.cache, t_b, dw.q, dw.qi, o, l, s, ws_t)
+        torch.cuda.synchronize()
+        assert msa.msa_read_device_error(ws_t) == 0
+        assert torch.equal(s, s_ref)
+        assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
