@@ -222,3 +222,47 @@ def test_inputs_written_by_the_kernel_just_before_are_seen():
         assert msa.msa_read_device_error(ws_t) == 0
         assert torch.equal(s, s_ref)
         assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
+@pytest.mark.parametrize("T,lens", [
+    (1, [20000, 9000, 3000, 129, 40000, 5000, 16 * 128 + 5, 700]),   # streaming indexer, team attention
+    (8, [30000, 70000, 2100]),                                       # tcgen05 speculative indexer
+    (96, [8000, 3000]),                                              # prefill indexer, block-major attention
+], ids=["decode", "spec", "prefill"])
+def test_page_relabelling_leaves_every_output_bitwise_unchanged(T, lens):
+    """The pages are reached only through the block table: moving every page of the six pools
+    to a new id (a seeded permutation) and rewriting the table to match leaves the block
+    scores, selections, outputs and lse bit-for-bit unchanged, on each indexer and attention
+    form."""
+    need_gpu()
+    import torch
+    import block_sparse_attention_indexer_gb300 as msa
+    w, lens = syn.custom(f"relabel_{T}", 141 + T, len(lens), T, 8, lens, shuffled=True)
+    dw = device_workload(w, lens)
+    B, H = w.batch, w.num_heads
+
+    def run(cache, batch):
+        out = torch.zeros(B, T, H, 128, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros(B, T, H, dtype=torch.float32, device="cuda")
+        sel = torch.zeros(B, T, 4, 16, dtype=torch.int32, device="cuda")
+        scores = torch.zeros(B, T, 4, batch.max_blocks, dtype=torch.float32, device="cuda")
+        ws = msa.alloc_workspace(msa.MSA_OP_DECODE, dw.cfg, batch)
+        ws_i = msa.alloc_workspace(msa.MSA_OP_INDEXER_SCORES, dw.cfg, batch)
+        msa.msa_decode(dw.cfg, cache, batch, dw.q, dw.qi, out, lse, sel, ws)
+        msa.msa_indexer_scores(dw.cfg, cache, batch, dw.qi, scores, ws_i)
+        torch.cuda.synchronize()
+        assert msa.msa_read_device_error(ws) == 0 and msa.msa_read_device_error(ws_i) == 0
+        return out, lse, sel, scores
+
+    base = run(dw.cache, dw.batch)
+    P = dw.cache.num_pages
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(5)).to("cuda")  # page p -> perm[p]
+    moved = msa.PagedCache(P, 4, 128, 128, 128)
+    for old, new in zip(dw.cache.tensors(), moved.tensors()):
+        new[perm] = old
+    tab = dw.batch.block_table
+    new_tab = torch.where(tab >= 0, perm[tab.clamp(min=0).long()].to(torch.int32), tab).contiguous()
+    assert not torch.equal(new_tab, tab)
+    relabelled = run(moved, msa.Batch(new_tab, dw.batch.seq_lens.clone(), T))
+    for name, a, b in zip(("out", "lse", "selection", "scores"), base, relabelled):
+        assert torch.equal(a, b), name
