@@ -77,6 +77,14 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def step_distribution(ms):
+    """Median, p10, p90, minimum and maximum of the per-step device times (ms)."""
+    import numpy as np
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)),
+            "min": float(a.min()), "max": float(a.max()), "n": int(a.size)}
+
+
 def measured_traffic(kernel: str, workload: str):
     """DRAM bytes (read + write) per launch from the committed ncu summary, or None when the
     kernel's sources changed since those counters were taken."""
@@ -299,7 +307,7 @@ def measure_workload(name, args, rank, dev, flush, peak, bf16_peak):
         torch.cuda.synchronize()
         return g.replay
 
-    def timed(fn, n):
+    def timed(fn, n, dist=None):
         run = graphed(fn)
         for _ in range(args.warmup):
             run()
@@ -310,12 +318,17 @@ def measure_workload(name, args, rank, dev, flush, peak, bf16_peak):
             run()
             b.record(stream)
         torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+        ms_list = [a.elapsed_time(b) for a, b in ev]
+        if dist is not None:
+            dist.extend(ms_list)
+        return statistics.mean(ms_list)
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
-    ms = timed(lambda: msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, lse, sel, wsp, None), args.steps)
+    step_list = []
+    ms = timed(lambda: msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, lse, sel, wsp, None), args.steps,
+               step_list)
     idx_ms = timed(lambda: msa.msa_indexer_scores(dw.cfg, dw.cache, dw.batch, dw.qi, scores, ws_idx, None),
                    args.steps)
     sel_ms = timed(lambda: msa.msa_select_blocks(dw.cfg, dw.batch, scores, sel, None), args.steps)
@@ -343,7 +356,7 @@ def measure_workload(name, args, rank, dev, flush, peak, bf16_peak):
                 "frac": gbs / peak, "algorithmic_bytes": idx_bytes, "traffic": measured_traffic(idx_kernel, name)}
     res = {"config": {"batch": B, "q_len": T, "heads": H, "mean_ctx": float(np.mean(dw.lens)),
                       "tokens_in_cache": int(np.sum(dw.lens))},
-           "ms_per_step": ms, "queries_per_s": queries / (ms / 1e3),
+           "ms_per_step": ms, "step_ms_dist": step_distribution(step_list), "queries_per_s": queries / (ms / 1e3),
            "step_roofline": {"bound": "hbm", "algorithmic_bytes": idx_bytes + kv_bytes, "achieved": step_gbs,
                              "unit": "GB/s", "frac": step_gbs / peak, "frac_of_8tbs": step_gbs / 8000.0},
            "roofline": roof,
@@ -567,7 +580,8 @@ def run_ours(args):
                     "peak_kind": f"{peak_kind} (burst copy)"}
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "step_ms_dist": step_distribution(step_ms),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "operands": "NVFP4 cache and FP8 queries widened exactly to f16", "data": "synthetic",
         "config": {"workload": w.name, "batch": B, "q_len": T, "heads": H, "kv_groups": 4, "head_dim": 128,
                    "index_dim": 128, "top_k": 16, "block": 128, "mean_ctx": float(np.mean(dw.lens)),
