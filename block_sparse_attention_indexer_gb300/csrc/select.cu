@@ -38,9 +38,10 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const SelectArgs
 // batches with few rows (decode: 4 warps, so that the row's loads and ranking are split
 // four ways instead of waiting on one warp).  Each warp takes the best of a contiguous
 // share of the candidates (the row's winners are among the union of the shares' winners,
-// at most NW x 16 keys); the first warp ranks those exact keys against each other -- each
-// lane holds NW / 2 of them and compares them with every key by shuffles -- and each of the
-// W winners writes its block id at its rank, then a warp sort puts them in ascending order.
+// at most NW x 16 keys, left in shared memory); the first warp ranks those exact keys -- each
+// lane holds NW / 2 of them and counts the larger keys, read back from shared memory as
+// broadcast 16-byte loads -- each of the W winners writes its block id at its rank, and each
+// then takes its ascending place, the number of winners with a smaller id.
 //
 // On the decode step (a.sel_pages set) the CTA also stages its sequence's block-table row in
 // shared memory and writes the page of every selected block, so that the attention kernel
