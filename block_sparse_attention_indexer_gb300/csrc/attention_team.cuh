@@ -309,11 +309,12 @@ __device__ __forceinline__ void attention_cta(const AttnArgs& a, uint8_t* smem, 
 }
 
 // Rows cut by team-range boundaries: combine the partial states the teams left.  One CTA per
-// boundary (the first boundary inside a row owns the row); its first warp lists the row's
-// partial slots in shared memory (arithmetic only, so it runs before the wait on the
-// attention kernel), then one thread per (head, pair of dims) loads the slots' states eight
-// at a time (a row has at most 16 slots, one per selection entry) and combines them; two
-// CTAs fit an SM, so the CTAs with no row to merge clear out in one wave.
+// boundary (the first boundary inside a row owns the row), or, with fewer rows than
+// boundaries, one per row (merge_kernel); its first warp lists the row's partial slots in
+// shared memory (arithmetic only, so it runs before the wait on the attention kernel), then
+// one thread per (head, pair of dims) loads the slots' states eight at a time (a row has at
+// most 16 slots, one per selection entry) and combines them; two CTAs fit an SM, so the CTAs
+// with no row to merge clear out in one wave.
 constexpr int kMergeThreads = kHeadsMax * kDim / 2;
 
 // The merge of the row cut by range boundary k (between team ranges k-1 and k) of NT, if k is
