@@ -266,3 +266,39 @@ def test_page_relabelling_leaves_every_output_bitwise_unchanged(T, lens):
     relabelled = run(moved, msa.Batch(new_tab, dw.batch.seq_lens.clone(), T))
     for name, a, b in zip(("out", "lse", "selection", "scores"), base, relabelled):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("T,lens", [(1, [9000, 300, 40000, 2200]), (8, [30000, 5000]), (80, [6000])],
+                         ids=["decode", "spec", "prefill"])
+def test_optional_outputs_change_nothing(T, lens):
+    """selection_out and lse are optional: with or without them msa_decode gives the same
+    output bit for bit (without selection_out the selection stays in the workspace), and the
+    selection it hands out is the one msa_select_blocks makes from the same scores."""
+    need_gpu()
+    import torch
+    import block_sparse_attention_indexer_gb300 as msa
+    w, lens = syn.custom(f"optional_{T}", 151 + T, len(lens), T, 8, lens, shuffled=True)
+    dw = device_workload(w, lens)
+    B, H = w.batch, w.num_heads
+    results = []
+    for with_sel, with_lse in ((True, True), (False, True), (True, False), (False, False)):
+        out = torch.zeros(B, T, H, 128, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros(B, T, H, dtype=torch.float32, device="cuda") if with_lse else None
+        sel = torch.full((B, T, 4, 16), 9, dtype=torch.int32, device="cuda") if with_sel else None
+        ws = msa.alloc_workspace(msa.MSA_OP_DECODE, dw.cfg, dw.batch)
+        msa.msa_decode(dw.cfg, dw.cache, dw.batch, dw.q, dw.qi, out, lse, sel, ws)
+        torch.cuda.synchronize()
+        assert msa.msa_read_device_error(ws) == 0
+        results.append((out, lse, sel))
+    for out, lse, sel in results[1:]:
+        assert torch.equal(out, results[0][0])
+        if lse is not None:
+            assert torch.equal(lse, results[0][1])
+    assert torch.equal(results[0][2], results[2][2])
+    scores = torch.zeros(B, T, 4, dw.batch.max_blocks, dtype=torch.float32, device="cuda")
+    msa.msa_indexer_scores(dw.cfg, dw.cache, dw.batch, dw.qi, scores,
+                           msa.alloc_workspace(msa.MSA_OP_INDEXER_SCORES, dw.cfg, dw.batch))
+    sel2 = torch.zeros(B, T, 4, 16, dtype=torch.int32, device="cuda")
+    msa.msa_select_blocks(dw.cfg, dw.batch, scores, sel2)
+    torch.cuda.synchronize()
+    assert torch.equal(sel2, results[0][2])
