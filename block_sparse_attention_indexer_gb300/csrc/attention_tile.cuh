@@ -68,9 +68,11 @@ __device__ __forceinline__ void attend_rows32(const uint8_t* kd, const uint8_t* 
   float x[2][4];
 #pragma unroll
   for (int mq = 0; mq < 2; ++mq) {
-    // tile row i holds key pi(i) = (i & 8) | (i & 1) << 2 | (i >> 1) & 3 of the 16: the PV
-    // step's lanes then read V rows 1 apart (2-way bank conflicts instead of 4-way)
-    const int i0 = mq * 16 + (((gq & 1) << 2) | (gq >> 1));
+    // tile row i holds key pi(i) = i ^ ((i >> 1) & 1) of the 16 (rows 0-7 and 8-15 alike): the
+    // two rows an 8-lane phase of the K loads reads then differ in parity (different bank
+    // halves of their 64-byte rows: no conflict), and each PV load reads two rows of each
+    // parity (its 2-way minimum)
+    const int i0 = mq * 16 + (gq ^ ((gq >> 1) & 1));
     const int r0 = rbase + i0, r1 = r0 + 8;
     const uint4 d0 = lds128(kd + r0 * kRowBytes + 16 * t4);
     const uint4 d1 = lds128(kd + r1 * kRowBytes + 16 * t4);
@@ -140,16 +142,15 @@ __device__ __forceinline__ void attend_rows32(const uint8_t* kd, const uint8_t* 
   for (int mq = 0; mq < 2; ++mq) {
     const uint32_t b0 = movmatrix_trans(pack_f16x2(p[mq][0], p[mq][1]));
     const uint32_t b1 = movmatrix_trans(pack_f16x2(p[mq][2], p[mq][3]));
-    // k-indices 2t4, 2t4+1, 2t4+8, 2t4+9 are keys pi(.) = t4, t4+4, t4+8, t4+12 of the tile
-    const int ka = rbase + mq * 16 + t4;
+    // k-indices 2t4, 2t4+1, 2t4+8, 2t4+9 are keys pi(.) = ka, kb, ka + 8, kb + 8 of the tile
+    const int ka = rbase + mq * 16 + ((2 * t4) ^ (t4 & 1)), kb = rbase + mq * 16 + ((2 * t4 + 1) ^ (t4 & 1));
     const uint2 va = lds64(vd + ka * kRowBytes + 8 * gq);
-    const uint2 vb = lds64(vd + (ka + 4) * kRowBytes + 8 * gq);
+    const uint2 vb = lds64(vd + kb * kRowBytes + 8 * gq);
     const uint2 vc = lds64(vd + (ka + 8) * kRowBytes + 8 * gq);
-    const uint2 ve = lds64(vd + (ka + 12) * kRowBytes + 8 * gq);
-    const uint32_t sab = e4m3x2_to_f16x2(lds8(vs + ka * kRowScales + gq) |
-                                         (lds8(vs + (ka + 4) * kRowScales + gq) << 8));
+    const uint2 ve = lds64(vd + (kb + 8) * kRowBytes + 8 * gq);
+    const uint32_t sab = e4m3x2_to_f16x2(lds8(vs + ka * kRowScales + gq) | (lds8(vs + kb * kRowScales + gq) << 8));
     const uint32_t scd = e4m3x2_to_f16x2(lds8(vs + (ka + 8) * kRowScales + gq) |
-                                         (lds8(vs + (ka + 12) * kRowScales + gq) << 8));
+                                         (lds8(vs + (kb + 8) * kRowScales + gq) << 8));
 #pragma unroll
     for (int hw = 0; hw < 2; ++hw) {
       const uint32_t wa = hw ? va.y : va.x, wb = hw ? vb.y : vb.x;
