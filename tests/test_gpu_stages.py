@@ -24,6 +24,12 @@ CASES = [
     ("hg4_t1", [4096] * 3, 1, 4, False),
     ("many_rows_t4", [300 + 37 * i for i in range(64)], 4, 8, True),     # 1024 rows: no split
     ("rows256_t2", [2500 + 101 * i for i in range(32)], 2, 8, True),      # 256 rows: 4 splits
+    # the dispatch edges: 64 rows (the GEMM indexer's first shape), 63 query tokens (the team
+    # attention's last), 64 query tokens (the block-major attention's first), each with a
+    # sequence exactly as long as its new tokens
+    ("edge_t16", [16, 700, 4000 + 9], 16, 8, True),
+    ("edge_t63", [63, 3000], 63, 8, True),
+    ("edge_t64", [64, 2000 + 3], 64, 8, True),
 ]
 
 
