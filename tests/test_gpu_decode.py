@@ -106,6 +106,17 @@ def test_prefill_4k_on_64k_sampled():
     _check(w, dw, tokens=toks)
 
 
+def test_one_million_token_context():
+    """A context of 1,048,576 + 77 tokens (8,193 blocks a row) next to a short one: more
+    candidates than the selection holds in registers (its shares are re-read from L2) and a
+    block-table row longer than it stages for the attention (which then looks the pages up
+    itself); every row checked against the oracle."""
+    need_gpu()
+    w, lens = syn.custom("ctx1m", 161, 2, 1, 8, [1048576 + 77, 20000], shuffled=True)
+    dw = device_workload(w, lens)
+    _check(w, dw)
+
+
 def test_deterministic_reruns():
     """Bitwise-identical reruns (a race would show up as nondeterminism)."""
     need_gpu()

@@ -30,6 +30,7 @@ CASES = [
     ("edge_t16", [16, 700, 4000 + 9], 16, 8, True),
     ("edge_t63", [63, 3000], 63, 8, True),
     ("edge_t64", [64, 2000 + 3], 64, 8, True),
+    ("prefill_hg4_t80", [80, 3000 + 1], 80, 4, True),       # block-major with 4 heads per group: 32 tokens a tile
 ]
 
 
