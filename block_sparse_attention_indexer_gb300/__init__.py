@@ -33,6 +33,7 @@ from .binding import (  # noqa: F401
     msa_select_blocks,
     msa_sparse_attn_decode,
     msa_sparse_attn_decode_noalloc,
+    msa_test_attention_stall,
     msa_test_indexer_stall,
     msa_workspace_bytes,
 )

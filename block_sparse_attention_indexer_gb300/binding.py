@@ -69,6 +69,8 @@ _SIGS = {
     "msa_sparse_attn_decode_noalloc": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P]),
     "msa_noalloc_read_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _P]),
     "msa_test_indexer_stall": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
+    "msa_test_attention_stall": (ctypes.c_int, [_CP, _CC, _CB, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32,
+                                                _P]),
     "msa_read_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "msa_clear_device_error": (ctypes.c_int, [_P, _P]),
 }
@@ -278,6 +280,17 @@ def msa_test_indexer_stall(cfg: Config, cache: PagedCache, batch: Batch, index_q
     _check("msa_test_indexer_stall", _lib.msa_test_indexer_stall(
         cfg.c(), cache.c(), batch.c(), _ptr(index_q, torch.uint8, "index_q"),
         _ptr(block_scores, torch.float32, "block_scores"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), spin_limit, _stream(stream)))
+
+
+def msa_test_attention_stall(cfg: Config, cache: PagedCache, batch: Batch, q: torch.Tensor, selection: torch.Tensor,
+                             out: torch.Tensor, lse: Optional[torch.Tensor], workspace: torch.Tensor, spin_limit: int,
+                             stream=None):
+    """Test hook: the team attention with its page copies withheld and every wait capped at
+    spin_limit polls (the waits run out; MSA_DEVERR_TIMEOUT is set)."""
+    _check("msa_test_attention_stall", _lib.msa_test_attention_stall(
+        cfg.c(), cache.c(), batch.c(), _ptr(q, torch.uint8, "q"), _ptr(selection, torch.int32, "selection"),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), spin_limit, _stream(stream)))
 
 

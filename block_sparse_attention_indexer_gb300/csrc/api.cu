@@ -409,6 +409,28 @@ msa_status_t msa_test_indexer_stall(const msa_config_t* cfg, const msa_cache_t* 
   return cuda_status(launch_indexer(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
+msa_status_t msa_test_attention_stall(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                      const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, uint32_t spin_limit, void* stream) {
+  msa_status_t st;
+  if ((st = check_config(cfg)) != MSA_OK || (st = check_batch(batch)) != MSA_OK ||
+      (st = check_cache(cache, false, true)) != MSA_OK)
+    return st;
+  if (batch->batch == 0) return MSA_OK;
+  if (spin_limit < 1 || spin_limit > kDefaultSpinLimit) return MSA_ERR_UNSUPPORTED;
+  if (q == nullptr || selection == nullptr || out == nullptr || !aligned16(q)) return MSA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < team_attn_workspace_bytes() || !aligned16(workspace))
+    return MSA_ERR_WORKSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MSA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AttnArgs a = attn_args(cfg, cache, batch, q, selection, out, lse, reinterpret_cast<float*>(ws + kErrBytes),
+                         reinterpret_cast<uint32_t*>(ws));
+  a.spin_limit = spin_limit;
+  a.test_withhold = 1;
+  return cuda_status(launch_attention(a, sms, static_cast<cudaStream_t>(stream)));
+}
+
 msa_status_t msa_read_device_error(const void* workspace, uint32_t* flags, void* stream) {
   if (workspace == nullptr || flags == nullptr) return MSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

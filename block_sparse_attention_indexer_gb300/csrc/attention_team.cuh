@@ -86,7 +86,9 @@ __device__ __forceinline__ bool send_item(const AttnArgs& a, int& produced, uint
       const int64_t pg = static_cast<int64_t>(page) * a.groups + row % a.groups;
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, kSlotBytes);
-      if (a.q_len == 1) {  // one token per sequence: every page is read once per call
+      if (a.test_withhold) {
+        // (test hook: no copy is issued, the slot never fills)
+      } else if (a.q_len == 1) {  // one token per sequence: every page is read once per call
         const uint64_t pol = l2_evict_first_policy();
         bulk_g2s_hint(dst, a.k_data + pg * kPageData, kPageData, bar, pol);
         bulk_g2s_hint(dst + kPageData, a.k_scale + pg * kPageScale, kPageScale, bar, pol);

@@ -63,6 +63,8 @@ struct AttnArgs {
   int32_t q_early;             // 1: read the first queries before waiting on the previous kernel
   uint32_t* err;
   uint32_t spin_limit;         // polls per bounded wait (team kernel)
+  int32_t test_withhold;       // test hook: the producers arm each page slot's byte count but
+                               // issue no copy, so the consumers' waits run out (team kernel)
 };
 
 struct QuantArgs {

@@ -287,6 +287,18 @@ msa_status_t msa_test_indexer_stall(const msa_config_t* cfg, const msa_cache_t* 
                                     const uint8_t* index_q, float* block_scores, void* workspace,
                                     size_t workspace_bytes, uint32_t spin_limit, void* stream);
 
+/* Test hook for the failure path of the team attention kernel's bounded waits; not part of
+ * the decode path.  Runs the query-major team attention of msa_sparse_attn_decode (whatever
+ * q_len; workspace of team size: msa_workspace_bytes(MSA_OP_SPARSE_ATTN, ...) for a batch below
+ * 64 query tokens) with every wait capped at spin_limit polls (1 .. 2^22) and the page copies
+ * withheld: each page slot is armed for its bytes but never filled, so the consumers' first
+ * waits run out, then the producers' waits for free slots.  Every wait ends, no copy is in
+ * flight when a wait gives up, MSA_DEVERR_TIMEOUT is set in the workspace error word and the
+ * launch returns; outputs are unspecified.  The context stays usable. */
+msa_status_t msa_test_attention_stall(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
+                                      const uint8_t* q, const int32_t* selection, uint16_t* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, uint32_t spin_limit, void* stream);
+
 /* Debug helper: copies the device error word out of `workspace` into *flags (this call
  * synchronises `stream`). */
 msa_status_t msa_read_device_error(const void* workspace, uint32_t* flags, void* stream);
