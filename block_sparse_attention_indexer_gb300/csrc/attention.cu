@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnAr
 // by_row 0: CTA i takes range boundary i + 1 (NT - 1 CTAs); by_row 1: CTA i takes row i (for
 // fewer rows than boundaries), through the first boundary inside it, if any: every CTA then
 // has a row to merge or leaves at once, and the grid does not outnumber the rows.
-__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const AttnArgs a, int NT, int by_row) {
+template <int kBatch>
+__global__ void __launch_bounds__(kMergeThreads, kBatch == 8 ? 2 : 1) merge_kernel(const AttnArgs a, int NT, int by_row) {
   __shared__ int s_slot[kTopK];
   __shared__ int s_n, s_row;
   int k = blockIdx.x + 1;
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const AttnArgs 
     if (owner_of(E, R * kTopK + kTopK - 1, NT) == ca) return;  // the row is one team's
     k = ca + 1;
   }
-  merge_boundary(a, NT, k, s_slot, &s_n, &s_row);
+  merge_boundary<kBatch>(a, NT, k, s_slot, &s_n, &s_row);
 }
 
 size_t attn_partial_bytes() {
@@ -88,7 +89,9 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s) {
   mcfg.stream = s;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&mcfg, merge_kernel, a, NT, by_row);
+  // a row's 16 slots in one round of loads when one CTA an SM still holds every row at once
+  e = by_row && rows <= NC ? cudaLaunchKernelEx(&mcfg, merge_kernel<16>, a, NT, by_row)
+                           : cudaLaunchKernelEx(&mcfg, merge_kernel<8>, a, NT, by_row);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -316,12 +316,14 @@ __device__ __forceinline__ void attention_cta(const AttnArgs& a, uint8_t* smem, 
 // shared memory (arithmetic only, so it runs before the wait on the attention kernel), then
 // one thread per (head, pair of dims) loads the slots' states eight at a time (a row has at
 // most 16 slots, one per selection entry) and combines them; two CTAs fit an SM, so the CTAs
-// with no row to merge clear out in one wave.
+// with no row to merge clear out in one wave.  With no more rows to merge than SMs, all 16 go
+// in one round (more registers, one CTA an SM: still a single wave).
 constexpr int kMergeThreads = kHeadsMax * kDim / 2;
 
 // The merge of the row cut by range boundary k (between team ranges k-1 and k) of NT, if k is
 // that row's first cut; kMergeThreads threads, scratch in shared memory (s_slot[16], s_n, s_row).
 // Ends with every thread past the CTA barrier, so that a CTA can take several boundaries in turn.
+template <int kBatch>
 __device__ __forceinline__ void merge_boundary(const AttnArgs& a, int NT, int k, int* s_slot, int* s_n, int* s_row) {
   const int tid = threadIdx.x, lane = tid & 31;
   __syncthreads();  // the scratch of a previous boundary is no longer read
@@ -358,9 +360,8 @@ __device__ __forceinline__ void merge_boundary(const AttnArgs& a, int NT, int k,
   const int h = tid / (kDim / 2), d = 2 * (tid % (kDim / 2));
   if (R < 0 || h >= a.heads_per_group) return;
   grid_dependency_wait();  // the attention kernel's partial states
-  // the slots' states are loaded eight at a time before any of them is used (one round of
-  // loads in flight per eight slots, not one per slot), then folded into the running sums
-  constexpr int kBatch = 8;
+  // the slots' states are loaded kBatch (8 or 16) at a time before any of them is used (one
+  // round of loads in flight per batch, not one per slot), then folded into the running sums
   float M = -INFINITY, num0 = 0.f, num1 = 0.f, den = 0.f;
   for (int i0 = 0; i0 < n; i0 += kBatch) {
     float ms[kBatch], ls[kBatch];
