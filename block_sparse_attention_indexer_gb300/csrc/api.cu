@@ -167,6 +167,9 @@ AttnArgs attn_args(const msa_config_t* cfg, const msa_cache_t* cache, const msa_
   a.scale_log2 = scale_log2(cfg);
   a.err = err;
   a.spin_limit = kDefaultSpinLimit;
+  a.top_k = cfg->top_k;
+  a.init_blocks = cfg->init_blocks;
+  a.local_blocks = cfg->local_blocks;
   return a;
 }
 
@@ -370,6 +373,18 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
                      : reinterpret_cast<int32_t*>(ws + kErrBytes + scores_bytes(cfg, batch));
   int32_t* pages = reinterpret_cast<int32_t*>(ws + kErrBytes + scores_bytes(cfg, batch) + sel_bytes(cfg, batch));
   uint8_t* scratch = ws + kErrBytes + scores_bytes(cfg, batch) + 2 * sel_bytes(cfg, batch);
+  AttnArgs aa = attn_args(cfg, cache, batch, q, sel, out, lse, reinterpret_cast<float*>(scratch), err);
+  aa.q_early = 1;  // the kernel before it is this step's selection, or its indexer
+  // a small batch of short rows: the attention's producers select their rows themselves (no
+  // selection launch between the indexer and the attention)
+  if (!block_major(cfg, batch) && rows_tg(batch, cfg) <= kFusedSelectMaxRows &&
+      batch->max_blocks <= kFusedSelectMaxBlocks) {
+    aa.block_scores = scores;
+    aa.sel_out = sel;
+    cudaError_t e = run_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
+    if (e == cudaSuccess) e = launch_attention(aa, sms, s);
+    return cuda_status(e);
+  }
   // the selection looks the selected pages up for the team attention kernel; the step's
   // inputs were written before its first kernel, which waited for them
   SelectArgs sa = select_args(cfg, batch, scores, sel);
@@ -380,8 +395,6 @@ msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const
   }
   cudaError_t e = run_indexer(indexer_args(cfg, cache, batch, index_q, scores, err), sms, s);
   if (e == cudaSuccess) e = launch_select(sa, s);
-  AttnArgs aa = attn_args(cfg, cache, batch, q, sel, out, lse, reinterpret_cast<float*>(scratch), err);
-  aa.q_early = 1;  // the kernel before it is this step's selection
   if (select_writes_pages(sa)) aa.sel_pages = pages;
   if (e == cudaSuccess) e = run_attention(cfg, batch, aa, scratch, sms, s, true);
   return cuda_status(e);

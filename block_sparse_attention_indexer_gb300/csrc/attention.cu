@@ -36,9 +36,10 @@
 
 namespace msa {
 
+template <bool kOwnSelect>
 __global__ void __launch_bounds__(kAttnThreads, 1) attention_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  attention_cta(a, smem, blockIdx.x, gridDim.x);
+  attention_cta<kOwnSelect>(a, smem, blockIdx.x, gridDim.x);
 }
 
 // by_row 0: CTA i takes range boundary i + 1 (NT - 1 CTAs); by_row 1: CTA i takes row i (for
@@ -67,7 +68,10 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const int NC = num_sms < kAttnMaxCtas ? num_sms : kAttnMaxCtas;
   const size_t smem = attn_smem_bytes();
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(attention_kernel), smem);
+  const bool own = a.block_scores != nullptr;
+  const void* kern = own ? reinterpret_cast<const void*>(attention_kernel<true>)
+                         : reinterpret_cast<const void*>(attention_kernel<false>);
+  cudaError_t e = ensure_dynamic_smem(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -79,7 +83,7 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attention_kernel, a);
+  e = own ? cudaLaunchKernelEx(&cfg, attention_kernel<true>, a) : cudaLaunchKernelEx(&cfg, attention_kernel<false>, a);
   if (e != cudaSuccess) return e;
   const int NT = NC * kTeams;
   const int by_row = rows < NT - 1 ? 1 : 0;

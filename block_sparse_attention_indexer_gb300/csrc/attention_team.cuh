@@ -6,6 +6,7 @@
 #include "attention_tile.cuh"
 #include "msa_device.cuh"
 #include "msa_kernels.h"
+#include "select_row.cuh"
 
 namespace msa {
 
@@ -35,8 +36,14 @@ constexpr size_t kBarsBytes = (static_cast<size_t>(kTeams) * sizeof(TeamBars) + 
 constexpr size_t kRedBytes = static_cast<size_t>(kAW) * kRedFloats * sizeof(float);
 static_assert(kSlotsBytes % 16 == 0 && kRedBytes % 16 == 0, "attention shared-memory regions must stay 16-byte aligned");
 
+// the producers' ranking scratch when they select rows themselves: 32 keys each, after the
+// item metadata (16-byte aligned: the ranking reads it back as 16-byte vectors)
+constexpr size_t kMetaBytes = static_cast<size_t>(kTeams) * kTSl * sizeof(ItemMeta);
+constexpr size_t kSelScratchOff = kSlotsBytes + kBarsBytes + kRedBytes + kMetaBytes;
+static_assert(kSelScratchOff % 16 == 0, "the selection scratch must be 16-byte aligned");
+
 __host__ __device__ constexpr size_t attn_smem_bytes() {
-  return kSlotsBytes + kBarsBytes + kRedBytes + static_cast<size_t>(kTeams) * kTSl * sizeof(ItemMeta);
+  return kSelScratchOff + static_cast<size_t>(kTeams) * 32 * sizeof(uint64_t);
 }
 
 // Team c of NC owns the entries [range_lo(c), range_lo(c + 1)) of the E = rows * 16 entries.
@@ -66,6 +73,29 @@ __device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int row) {
   ri.ok = ri.L > 0 && ri.L >= a.q_len && ri.L <= static_cast<int64_t>(a.max_blocks) * kBlock;
   ri.r = ri.ok ? (ri.L - a.q_len + ri.t) / kBlock : -1;
   return ri;
+}
+
+// A producer's own selection of row R (the decode step of a small batch): the row's blocks
+// chosen from its block scores with the selection kernels' total order (select_row_warp:
+// higher score first, lower block on ties, the forced blocks), so the selection is the one
+// msa_select_blocks makes; written out when `own` (the team holds the row's first entry),
+// then resolved to pages like a read selection.  cb: 32 keys of shared scratch.
+__device__ __forceinline__ void select_resolve(const AttnArgs& a, int R, int lane, uint64_t* cb, bool own, int& blk,
+                                               int& page, int& pos) {
+  const unsigned TG = static_cast<unsigned>(a.q_len * a.groups);
+  const int b = static_cast<int>(static_cast<unsigned>(R) / TG);
+  const int t = static_cast<int>((static_cast<unsigned>(R) - static_cast<unsigned>(b) * TG) /
+                                 static_cast<unsigned>(a.groups));
+  RowRaw raw;
+  raw.L = a.seq_lens[b];
+  raw.page = -1;
+  const bool ok = raw.L > 0 && raw.L >= a.q_len && raw.L <= static_cast<int64_t>(a.max_blocks) * kBlock;
+  raw.blk = ok ? select_row_warp<8>(a.block_scores + static_cast<int64_t>(R) * a.max_blocks,
+                                    (raw.L - a.q_len + t) / kBlock, a.top_k, a.init_blocks, a.local_blocks, lane,
+                                    nullptr, 0, cb, 32)
+               : -1;
+  if (own && lane < kTopK) a.sel_out[static_cast<int64_t>(R) * kTopK + lane] = raw.blk;
+  row_resolve(a, R, raw, lane, blk, page, pos);
 }
 
 // Sends one item into the team's next slot once its four warps have released it: a page
@@ -110,6 +140,9 @@ __device__ __forceinline__ bool send_item(const AttnArgs& a, int& produced, uint
 
 // One CTA of the persistent team attention (CTA cta of ncta; kAttnThreads threads, the dynamic
 // shared memory of attn_smem_bytes() at smem).
+// kOwnSelect: the producers select their rows themselves (a.block_scores set); a separate
+// instance, so that the common path compiles without the selection code.
+template <bool kOwnSelect>
 __device__ __forceinline__ void attention_cta(const AttnArgs& a, uint8_t* smem, int cta, int ncta) {
   TeamBars* tbars = reinterpret_cast<TeamBars*>(smem + kSlotsBytes);
   float* red = reinterpret_cast<float*>(smem + kSlotsBytes + kBarsBytes);
@@ -151,14 +184,19 @@ __device__ __forceinline__ void attention_cta(const AttnArgs& a, uint8_t* smem, 
     int produced = 0;
     bool ok = true;
     const int R_last = (x1 - 1) / kTopK;
+    uint64_t* sel_cb = reinterpret_cast<uint64_t*>(smem + kSelScratchOff) + tm * 32;
     RowRaw raw = {};
-    if (x0 < x1) raw = row_fetch(a, x0 / kTopK, lane);
+    if (x0 < x1 && !kOwnSelect) raw = row_fetch(a, x0 / kTopK, lane);
     for (int R = x0 / kTopK; x0 < x1 && R <= R_last && ok; ++R) {
-      RowRaw next = {};
-      if (R < R_last) next = row_fetch(a, R + 1, lane);  // in flight while row R is sent
       int blk, page, pos;
-      row_resolve(a, R, raw, lane, blk, page, pos);
-      raw = next;
+      if (kOwnSelect) {
+        select_resolve(a, R, lane, sel_cb, R * kTopK >= x0, blk, page, pos);
+      } else {
+        RowRaw next = {};
+        if (R < R_last) next = row_fetch(a, R + 1, lane);  // in flight while row R is sent
+        row_resolve(a, R, raw, lane, blk, page, pos);
+        raw = next;
+      }
       const int j0 = max(x0 - R * kTopK, 0), j1 = min(x1 - R * kTopK, kTopK);
       bool any = false;
       for (int j = j0; j < j1 && ok; ++j) {

@@ -65,7 +65,16 @@ struct AttnArgs {
   uint32_t spin_limit;         // polls per bounded wait (team kernel)
   int32_t test_withhold;       // test hook: the producers arm each page slot's byte count but
                                // issue no copy, so the consumers' waits run out (team kernel)
+  // decode step of a small batch (else null): the producers select each row's blocks from its
+  // scores ([B][T][G][max_blocks]) themselves instead of reading `selection`; the team holding
+  // a row's first entry writes the row's selection to sel_out
+  const float* block_scores;
+  int32_t* sel_out;
+  int32_t top_k, init_blocks, local_blocks;
 };
+// the producers' own selection: at most this many rows of at most this many blocks
+constexpr int kFusedSelectMaxRows = 128;
+constexpr int kFusedSelectMaxBlocks = 256;
 
 struct QuantArgs {
   const float* x;

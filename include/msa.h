@@ -239,7 +239,11 @@ msa_status_t msa_sparse_attn_decode(const msa_config_t* cfg, const msa_cache_t* 
  * team attention kernel) and the stage-3 scratch (the stage-3 form follows the same 64-token
  * rule as msa_sparse_attn_decode).  seq_lens and block_table are read from the selection
  * kernel's start, before the indexer has finished: like q and index_q, they must be written
- * before the call's first kernel runs (any earlier stream-ordered write is). */
+ * before the call's first kernel runs (any earlier stream-ordered write is).  For a small
+ * batch of short rows (at most 128 (token, group) rows of at most 256 blocks, below 64 query
+ * tokens) there is no selection kernel: the attention kernel's producers select their rows
+ * from the block scores themselves, with the same order (the selection, written to
+ * selection_out or the workspace, is the one msa_select_blocks makes). */
 msa_status_t msa_decode(const msa_config_t* cfg, const msa_cache_t* cache, const msa_batch_t* batch,
                         const uint8_t* q, const uint8_t* index_q, uint16_t* out, float* lse,
                         int32_t* selection_out, void* workspace, size_t workspace_bytes, void* stream);
