@@ -68,6 +68,21 @@ def indexer_kernel_for(q_len: int, groups: int) -> str:
     return "spec_indexer_kernel" if rows < 64 else "prefill_indexer_kernel"
 
 
+def decode_path(batch: int, q_len: int, groups: int, max_blocks: int):
+    """The attention form msa_decode takes and the kernels it launches per step.
+
+    From 64 query tokens on: the block-major attention (CSR count, scan and scatter, f16
+    queries, tcgen05 block attention, log-sum-exp merge) after the indexer and the selection.
+    A small batch (at most 128 token x group rows of at most 256 blocks): the indexer, the
+    attention whose producers select their rows, and the merge.  Otherwise the indexer, the
+    selection, the team attention and its merge.
+    """
+    if q_len >= 64:
+        return "block-major (K-to-Q CSR, tcgen05)", 8
+    if batch * q_len * groups <= 128 and max_blocks <= 256:
+        return "query-major teams (mma.sync), selection in the attention's producers", 3
+    return "query-major teams (mma.sync)", 4
+
 def kernel_source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
@@ -345,6 +360,7 @@ def measure_workload(name, args, rank, dev, flush, peak, bf16_peak):
     vis = np.clip(pos[:, :, None, None] - 128 * sel_h.astype(np.int64) + 1, 0, 128) * (sel_h >= 0)
     att_flops = 4.0 * 128 * (H // 4) * float(np.sum(vis))
     idx_kernel = indexer_kernel_for(T, 4)
+    form, n_launch = decode_path(B, T, 4, dw.batch.max_blocks)
     if idx_kernel == "prefill_indexer_kernel":
         idx_flops = 2.0 * 128 * 4 * float(np.sum(pos + 1))
         tf = idx_flops / (idx_ms / 1e3) / 1e12
@@ -362,9 +378,9 @@ def measure_workload(name, args, rank, dev, flush, peak, bf16_peak):
            "roofline": roof,
            "stages_ms": {"indexer": idx_ms, "select": sel_ms, "attention": att_ms,
                          "attention_gbs": kv_bytes / (att_ms / 1e3) / 1e9, "attention_bytes": kv_bytes},
-           "attention_form": "block-major (K-to-Q CSR, tcgen05)" if T >= 64 else "query-major teams (mma.sync)",
+           "attention_form": form,
            "attention_tflops": att_flops / (att_ms / 1e3) / 1e12,
-           "launches_per_step": 8 if T >= 64 else 4,
+           "launches_per_step": n_launch,
            "clocks": clk, "setup_s": round(setup_s, 1)}
     del dw, out, lse, sel, wsp, scores, ws_idx, ws_att
     torch.cuda.empty_cache()
@@ -553,11 +569,8 @@ def run_ours(args):
     idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
     att_gbs = kv_bytes / (att_ms / 1e3) / 1e9
     step_gbs = (idx_bytes + kv_bytes) / (ms_step / 1e3) / 1e9
-    # indexer, select, then the team attention and its partial merge, or (from 64 query tokens
-    # on) the block-major attention: CSR count, scan and scatter, f16 queries, tcgen05 block
-    # attention, log-sum-exp merge (its counter memset is not a kernel)
-    block_major = T >= 64
-    launches_per_step = 8 if block_major else 4
+    # the block-major form's counter memset is not a kernel
+    form, launches_per_step = decode_path(B, T, 4, dw.batch.max_blocks)
     # attention FLOPs: QK and PV, 2 * 128 each, per (query head, visible selected key)
     pos_bt = dw.lens[:, None] - T + np.arange(T)[None, :]
     vis = np.clip(pos_bt[:, :, None, None] - 128 * sel_h.astype(np.int64) + 1, 0, 128) * (sel_h >= 0)
@@ -595,7 +608,7 @@ def run_ours(args):
         "roofline": roofline,
         "stages_ms": {"indexer": idx_ms, "select": sel_ms, "attention": att_ms,
                       "attention_gbs": att_gbs, "attention_bytes": kv_bytes},
-        "attention_form": "block-major (K-to-Q CSR, tcgen05)" if block_major else "query-major teams (mma.sync)",
+        "attention_form": form,
         "attention_tflops": att_flops / (att_ms / 1e3) / 1e12,
         "e2e": {"value": ws * queries / e2e_s, "unit": "queries/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
