@@ -260,8 +260,10 @@ msa_status_t msa_nvfp4_insert(const float* x, int64_t n_tokens, int32_t rows_per
   if (x == nullptr || slots == nullptr || data == nullptr || scale == nullptr || !aligned16(x) ||
       (reinterpret_cast<uintptr_t>(data) & 7u) != 0)
     return MSA_ERR_INVALID_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MSA_ERR_CUDA;
   QuantArgs a{x, n_tokens, rows_per_token, dim, slots, data, scale, num_pages, block_size};
-  return cuda_status(launch_nvfp4_insert(a, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_nvfp4_insert(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 msa_status_t msa_fp8_quantize(const float* x, int64_t n, uint8_t* out, void* stream) {

@@ -92,7 +92,7 @@ struct QuantArgs {
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
 // Launchers return cudaGetLastError() after enqueueing.
-cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s);
+cudaError_t launch_nvfp4_insert(const QuantArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_fp8_quantize(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
 cudaError_t launch_indexer(const IndexerArgs& a, int num_sms, cudaStream_t s);
 // tcgen05 GEMM form of the indexer for long query chunks (chunked prefill)

@@ -49,75 +49,109 @@ __device__ __forceinline__ float div_rn_by_recip(float x, float d, float y) {
   return copysignf(__fmaf_rn(r, y, q), x);
 }
 
-// One thread per 16-element group; a warp takes whole tokens: 32 / groups-per-token tokens at
-// a time when a token has at most 32 groups (lane -> (token, group)), else one token with its
-// groups strided over the lanes.  Consecutive lanes read consecutive 64-byte groups
-// (coalesced), and the index arithmetic is 32-bit: the token's slot splits into (page,
-// offset) with one 32-bit division whenever the pool's slot count fits.
-__global__ void nvfp4_insert_kernel(QuantArgs a, int tpw) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int gpr = a.dim / 16;                // groups per row
-  const int gpt = a.rows_per_token * gpr;    // groups per token
-  const int span = tpw * gpt;                // groups per warp pass
+// The 16 inputs and the slot of group gt (= row * groups-per-row + grp) of token tok.  The
+// inputs are read once: streaming loads (evict first), issued together with the slot's.
+__device__ __forceinline__ void insert_load(const QuantArgs& a, int64_t tok, int64_t first, float4 (&v)[4],
+                                            int64_t& slot) {
+  const float4* src = reinterpret_cast<const float4*>(a.x) + 4 * first;
+  slot = __ldg(a.slots + tok);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = __ldcs(src + j);
+}
+
+// Encodes one group and writes its 8 code bytes and its scale into the token's slot (nothing
+// for a slot outside the pool).
+__device__ __forceinline__ void insert_store(const QuantArgs& a, int gt, int gpr, const float4 (&in)[4], int64_t slot,
+                                             int64_t cap, bool slots32) {
+  if (slot < 0 || slot >= cap) return;
+  const float v[16] = {in[0].x, in[0].y, in[0].z, in[0].w, in[1].x, in[1].y, in[1].z, in[1].w,
+                       in[2].x, in[2].y, in[2].z, in[2].w, in[3].x, in[3].y, in[3].z, in[3].w};
+  const int row = static_cast<int>(static_cast<uint32_t>(gt) / static_cast<uint32_t>(gpr));
+  const int grp = gt - row * gpr;
+  int64_t page;
+  int off;
+  if (slots32) {
+    const uint32_t s32 = static_cast<uint32_t>(slot), bs = static_cast<uint32_t>(a.block_size);
+    const uint32_t p32 = s32 / bs;
+    page = p32;
+    off = static_cast<int>(s32 - p32 * bs);
+  } else {
+    page = slot / a.block_size;
+    off = static_cast<int>(slot - page * a.block_size);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  // the divisions are correctly rounded either way; an infinite element (amax = inf) takes
+  // the plain division, whose result the reciprocal form would turn into NaN
+  const bool finite = isfinite(amax);
+  constexpr float kInv6 = 1.0f / 6.0f;  // RN(1/6)
+  const uint32_t scode = f32_to_e4m3(finite ? div_rn_by_recip(amax, 6.0f, kInv6) : __fdiv_rn(amax, 6.0f));
+  const float scale = e4m3_to_f32(scode);
+  uint2 packed = make_uint2(0u, 0u);
+  if (scale > 0.0f) {
+    float r[16];
+    if (finite) {
+      const float inv = __frcp_rn(scale);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) r[j] = div_rn_by_recip(v[j], scale, inv);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) r[j] = __fdiv_rn(v[j], scale);
+    }
+    packed.x = f32x8_to_e2m1x8(r);
+    packed.y = f32x8_to_e2m1x8(r + 8);
+  }
+  const int64_t row_index = (page * a.rows_per_token + row) * a.block_size + off;
+  *reinterpret_cast<uint2*>(a.data + row_index * (a.dim / 2) + grp * 8) = packed;
+  a.scale[row_index * gpr + grp] = static_cast<uint8_t>(scode);
+}
+
+// One thread per 16-element group.  The groups of all tokens are numbered token-major (group
+// gt of token tok is tok * groups-per-token + gt), so group g's inputs are the 64 bytes at
+// x + 64 g: consecutive threads read consecutive bytes.  A grid of kInsertCtasPerSm CTAs an SM
+// strides over the groups, and each thread loads its next group before it encodes the current
+// one, so that its loads stay in flight while it computes; (token, gt) advance by the stride's
+// quotient and remainder instead of a division per group.
+constexpr int kInsertThreads = 256;
+constexpr int kInsertCtasPerSm = 4;
+
+__global__ void __launch_bounds__(kInsertThreads, kInsertCtasPerSm) nvfp4_insert_kernel(QuantArgs a) {
+  const int gpr = a.dim / 16;              // groups per row
+  const int gpt = a.rows_per_token * gpr;  // groups per token
+  const int64_t total = a.n_tokens * gpt;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= total) return;
   const int64_t cap = a.num_pages * a.block_size;
   const bool slots32 = cap <= 0x7fffffff;
-  for (int64_t t0 = warp * tpw; t0 < a.n_tokens; t0 += nwarps * tpw) {
-    for (int i = lane; i < span; i += 32) {
-      const int sub = i / gpt, gt = i - sub * gpt;
-      const int64_t tok = t0 + sub;
-      if (tok >= a.n_tokens) continue;
-      const int row = gt / gpr, grp = gt - row * gpr;
-      // the group's 64 input bytes do not depend on the slot: both loads go out together
-      const int64_t slot = __ldg(a.slots + tok);
-      const float4* src = reinterpret_cast<const float4*>(a.x + (tok * a.rows_per_token + row) * a.dim + grp * 16);
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 f = __ldg(src + j);
-        v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
-      }
-      if (slot < 0 || slot >= cap) continue;
-      int64_t page;
-      int off;
-      if (slots32) {
-        const uint32_t s32 = static_cast<uint32_t>(slot), bs = static_cast<uint32_t>(a.block_size);
-        const uint32_t p32 = s32 / bs;
-        page = p32;
-        off = static_cast<int>(s32 - p32 * bs);
-      } else {
-        page = slot / a.block_size;
-        off = static_cast<int>(slot - page * a.block_size);
-      }
-
-      float amax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
-      // the divisions are correctly rounded either way; an infinite element (amax = inf) takes
-      // the plain division, whose result the reciprocal form would turn into NaN
-      const bool finite = isfinite(amax);
-      constexpr float kInv6 = 1.0f / 6.0f;  // RN(1/6)
-      const uint32_t scode = f32_to_e4m3(finite ? div_rn_by_recip(amax, 6.0f, kInv6) : __fdiv_rn(amax, 6.0f));
-      const float scale = e4m3_to_f32(scode);
-      uint2 packed = make_uint2(0u, 0u);
-      if (scale > 0.0f) {
-        float r[16];
-        if (finite) {
-          const float inv = __frcp_rn(scale);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) r[j] = div_rn_by_recip(v[j], scale, inv);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) r[j] = __fdiv_rn(v[j], scale);
-        }
-        packed.x = f32x8_to_e2m1x8(r);
-        packed.y = f32x8_to_e2m1x8(r + 8);
-      }
-      const int64_t row_index = (page * a.rows_per_token + row) * a.block_size + off;
-      *reinterpret_cast<uint2*>(a.data + row_index * (a.dim / 2) + grp * 8) = packed;
-      a.scale[row_index * gpr + grp] = static_cast<uint8_t>(scode);
+  const int64_t dq = stride / gpt;
+  const int dr = static_cast<int>(stride - dq * gpt);
+  int64_t tok = g / gpt;
+  int gt = static_cast<int>(g - tok * gpt);
+  float4 cur[4];
+  int64_t slot;
+  insert_load(a, tok, g, cur, slot);
+  for (;;) {
+    const int64_t gn = g + stride;
+    int64_t tokn = tok + dq;
+    int gtn = gt + dr;
+    if (gtn >= gpt) {
+      gtn -= gpt;
+      ++tokn;
     }
+    const bool more = gn < total;
+    float4 nxt[4];
+    int64_t slotn = -1;
+    if (more) insert_load(a, tokn, gn, nxt, slotn);
+    insert_store(a, gt, gpr, cur, slot, cap, slots32);
+    if (!more) break;
+    g = gn;
+    tok = tokn;
+    gt = gtn;
+    slot = slotn;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
   }
 }
 
@@ -127,14 +161,13 @@ __global__ void fp8_quantize_kernel(const float* __restrict__ x, int64_t n, uint
     out[i] = static_cast<uint8_t>(f32_to_e4m3(x[i]));
 }
 
-cudaError_t launch_nvfp4_insert(const QuantArgs& a, cudaStream_t s) {
+cudaError_t launch_nvfp4_insert(const QuantArgs& a, int num_sms, cudaStream_t s) {
   if (a.n_tokens == 0) return cudaSuccess;
-  const int gpt = a.rows_per_token * (a.dim / 16);
-  const int tpw = gpt >= 32 ? 1 : 32 / gpt;  // tokens per warp pass
-  const int threads = 256;
-  const int64_t warps = (a.n_tokens + tpw - 1) / tpw;
-  const int64_t blocks = (warps + threads / 32 - 1) / (threads / 32);
-  nvfp4_insert_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0, s>>>(a, tpw);
+  const int64_t total = a.n_tokens * a.rows_per_token * (a.dim / 16);
+  const int64_t needed = (total + kInsertThreads - 1) / kInsertThreads;
+  const int64_t resident = static_cast<int64_t>(num_sms) * kInsertCtasPerSm;
+  const int64_t blocks = needed < resident ? needed : resident;
+  nvfp4_insert_kernel<<<static_cast<unsigned>(blocks), kInsertThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

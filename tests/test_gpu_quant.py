@@ -55,6 +55,38 @@ def test_nvfp4_insert_bit_exact():
     assert np.array_equal(to_np(data), d_gpu)
 
 
+def test_nvfp4_insert_many_passes_odd_shape():
+    """A write larger than one pass of the grid, with groups per token (3 rows x 5 groups)
+    that do not divide the grid's thread count: each thread's (token, group) advances across
+    passes with a carry; every token's codes and scales are compared with the oracle."""
+    need_gpu()
+    import torch
+    import block_sparse_attention_indexer_gb300 as msa
+    rng = np.random.default_rng(11)
+    R, D, BL = 3, 80, 64
+    n = 40_000
+    P = (n + BL - 1) // BL + 5
+    x = (rng.standard_normal((n, R, D)) * rng.uniform(0.01, 50, (n, 1, 1))).astype(np.float32)
+    x[7] = -0.0
+    x[n - 1, 2, 64:] = np.inf
+    slots = rng.permutation(P * BL)[:n].astype(np.int64)
+    slots[123] = -5                                  # skipped
+    data = torch.zeros(P, R, BL, D // 2, dtype=torch.uint8, device="cuda")
+    scale = torch.zeros(P, R, BL, D // 16, dtype=torch.uint8, device="cuda")
+    msa.msa_nvfp4_insert(torch.from_numpy(x).cuda(), torch.from_numpy(slots).cuda(), data, scale, BL)
+    torch.cuda.synchronize()
+    d_ref, s_ref = OF.nvfp4_quantize(x)              # [n, R, 40], [n, R, 5]
+    d_gpu, s_gpu = to_np(data), to_np(scale)
+    ok = slots >= 0
+    p, o = np.divmod(slots[ok], BL)
+    assert np.array_equal(d_gpu[p, :, o], d_ref[ok])
+    assert np.array_equal(s_gpu[p, :, o], s_ref[ok])
+    used = np.zeros(P * BL, bool)
+    used[slots[ok]] = True
+    flat = s_gpu.transpose(0, 2, 1, 3).reshape(P * BL, -1)
+    assert (flat[~used] == 0).all()
+
+
 def test_nvfp4_insert_index_layout():
     need_gpu()
     import torch
