@@ -309,8 +309,9 @@ __device__ __forceinline__ int select_row_warp(const float* s, int r, int top_k,
 
 // The selection of one row by NW warps (all of them call it, with the same row and the row's
 // sequence length L, read by the caller): each warp takes the best of a contiguous share of the
-// candidates, then the first warp ranks the shares' winners by the exact keys they left in
-// shared memory.  sync() is a barrier over the NW warps; buf / part / win_ids are their shared
+// candidates, then every thread counts, for one of the shares' winners, the larger of the exact
+// keys they left in shared memory over one half of them (a single warp ranking them all waited
+// on its own chain of shared loads), and the first warp orders the row's winners.  sync() is a barrier over the NW warps; buf / part / win_ids are their shared
 // scratch (buf[NW][kSelCap / 8], part[NW][16], win_ids[16]).  If a.sel_pages is set the page of
 // every selected block is written beside it, from tab (the sequence's block-table row in shared
 // memory) or, if tab is null, from a.block_table.
@@ -318,7 +319,8 @@ template <int NW, int KPL, typename Sync>
 __device__ __forceinline__ void select_split_row(const SelectArgs& a, int64_t row, int L, int warp, int lane,
                                                  uint64_t (*buf)[kSelCap / 8], uint64_t (*part)[kTopK],
                                                  int32_t* win_ids, const int32_t* tab, Sync sync) {
-  constexpr int kKeys = NW * kTopK / 32;  // candidate keys per lane in the final ranking
+  constexpr int kNK = NW * kTopK;  // the shares' winner keys, ranked by 2 x NW x 32 threads
+  static_assert(2 * kNK == NW * 32, "two threads per key");
   const int b = static_cast<int>(row / (static_cast<int64_t>(a.q_len) * a.groups));
   const int t = static_cast<int>((row / a.groups) % a.q_len);
   int32_t* out = a.selection + row * kTopK;
@@ -353,24 +355,28 @@ __device__ __forceinline__ void select_split_row(const SelectArgs& a, int64_t ro
     part[warp][lane] = rec == kNoWinner ? 0ull
                                         : (rec << 32) | static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(rec >> 32));
   sync();
-  if (warp != 0) return;
-  uint64_t key[kKeys];
+  // rank of each of the NK shares' winners = keys larger than it (all keys distinct), counted
+  // by two threads per key over one half of the keys each, the keys read back two at a time;
+  // the per-warp survivor buffers are free now and take the upper halves' counts
+  const int tid = warp * 32 + lane;
+  const int h = tid / kNK, i = tid - h * kNK;
+  const uint64_t key = (&part[0][0])[i];
+  int cnt = 0;
+  const ulonglong2* half = reinterpret_cast<const ulonglong2*>(&part[0][0]) + h * (kNK / 4);
 #pragma unroll
-  for (int i = 0; i < kKeys; ++i) key[i] = (&part[0][0])[32 * i + lane];
-  // rank of each key = keys larger than it (all keys distinct), the keys read two at a time
-  int rank[kKeys];
-#pragma unroll
-  for (int i = 0; i < kKeys; ++i) rank[i] = 0;
-#pragma unroll
-  for (int j = 0; j < NW * kTopK / 2; ++j) {
-    const ulonglong2 x = reinterpret_cast<const ulonglong2*>(&part[0][0])[j];
-#pragma unroll
-    for (int i = 0; i < kKeys; ++i) rank[i] += (x.x > key[i] ? 1 : 0) + (x.y > key[i] ? 1 : 0);
+  for (int j = 0; j < kNK / 4; ++j) {
+    const ulonglong2 x = half[j];
+    cnt += (x.x > key ? 1 : 0) + (x.y > key ? 1 : 0);
   }
-#pragma unroll
-  for (int i = 0; i < kKeys; ++i)
-    if (key[i] != 0ull && rank[i] < W) win_ids[rank[i]] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key[i]));
-  __syncwarp();
+  int32_t* cnt_hi = reinterpret_cast<int32_t*>(&buf[0][0]);
+  if (h == 1) cnt_hi[i] = cnt;
+  sync();
+  if (h == 0) {
+    const int rank = cnt + cnt_hi[i];
+    if (key != 0ull && rank < W) win_ids[rank] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
+  }
+  sync();
+  if (warp != 0) return;
   // ascending order: each winner's place = winners with a smaller block id
   const int my_id = lane < W ? win_ids[lane] : 0x7fffffff;
   int at = 0;
