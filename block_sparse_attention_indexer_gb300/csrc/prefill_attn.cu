@@ -12,10 +12,13 @@
 //
 // Launches, each a programmatic dependent of the one before:
 //   1. the plan (K-to-Q CSR of every (sequence, KV group)): a memset of the block counters,
-//      bm_count_kernel (one thread per (token, group, slot) entry: the block's counter; a slot
-//      without a block gets the empty state m = -inf for every head), bm_scan_kernel (one CTA
-//      per (sequence, group): exclusive prefix of the counts into offsets and insertion
-//      cursors) and bm_scatter_kernel (every valid entry t * 16 + slot into its block's list);
+//      bm_count_kernel (a CTA per chunk of 128 query tokens of a (sequence, group): its
+//      entries' blocks counted in a shared-memory histogram, then one atomic per block; a slot
+//      without a block gets the empty state m = -inf for every head; the launch's other CTAs
+//      widen the FP8 queries to f16), bm_scan_kernel (one CTA per (sequence, group): exclusive
+//      prefix of the counts into offsets and insertion cursors) and bm_scatter_kernel (every
+//      valid entry t * 16 + slot into its block's list, a chunk's run of each list reserved
+//      with one atomic);
 //   2. bm_attn_kernel, persistent, one CTA per SM, on the tcgen05 tensor cores.  A work unit
 //      is one (sequence, group, block) with entries.  Loader warps copy the block's K and V
 //      pages (18 KB of E2M1 + E4M3 scales, one bulk copy a unit ahead) and dequantise them
@@ -67,25 +70,86 @@ __device__ __forceinline__ int bm_entry_block(const AttnArgs& a, int b, int g, i
   return n;
 }
 
-// Plan, count: one thread per (token, group, slot) entry; slots without a block get the
-// empty state (m = -inf) for every head of the group.
-__global__ void __launch_bounds__(kBmThreads) bm_count_kernel(const AttnArgs a, BmWorkspace w) {
+// The plan kernels take a (sequence, group) in chunks of kPlanTokens query tokens, one CTA per
+// chunk, kPlanPer entries (token, slot) per thread.  A chunk's block counts are first gathered
+// in a shared-memory histogram (its 128 tokens all select their own recent block, and popular
+// blocks are chosen by many), so a global counter takes one atomic per chunk instead of one
+// per entry; rows of more than kPlanHistMax blocks count with global atomics directly.
+constexpr int kPlanTokens = 128;
+constexpr int kPlanPer = kPlanTokens * kTopK / kBmThreads;  // 8
+constexpr int kPlanHistMax = 12288;                         // 48 KB of shared memory
+
+__device__ __forceinline__ int plan_chunks(const AttnArgs& a) { return (a.q_len + kPlanTokens - 1) / kPlanTokens; }
+
+// The block of each of this thread's entries of chunk `c` (-1: none), entry k = (token t0 +
+// (threadIdx.x + k * kBmThreads) / 16, slot (threadIdx.x + k * kBmThreads) % 16).
+__device__ __forceinline__ void plan_entries(const AttnArgs& a, int c, int& bg, int& t0, int (&n)[kPlanPer]) {
+  const int chunks = plan_chunks(a);
+  bg = c / chunks;
+  t0 = (c - bg * chunks) * kPlanTokens;
+  const int b = bg / a.groups, g = bg - b * a.groups;
+  const int L = a.seq_lens[b];
+  const bool ok = L > 0 && L >= a.q_len && L <= static_cast<int64_t>(a.max_blocks) * kBlock;
+#pragma unroll
+  for (int k = 0; k < kPlanPer; ++k) {
+    const int e = threadIdx.x + k * kBmThreads, t = t0 + e / kTopK;
+    n[k] = t < a.q_len ? bm_entry_block(a, b, g, t, e % kTopK, L, ok) : -1;
+  }
+}
+
+// Plan, count (CTAs 0 .. count_ctas - 1): each chunk's block counts into the counters, and the
+// empty state (m = -inf for every head of the group) for each slot without a block.  The
+// CTAs after them widen the FP8 queries to f16 (exact), 16 values per thread: the block
+// attention gathers query rows from this copy with asynchronous 16-byte copies straight into
+// its swizzled tiles.  (The widening needs nothing of the plan; it shares the launch so that it
+// runs beside the counting.)
+__global__ void __launch_bounds__(kBmThreads) bm_count_kernel(const AttnArgs a, BmWorkspace w, int count_ctas) {
+  extern __shared__ int32_t hist[];  // [max_blocks] when max_blocks <= kPlanHistMax
   grid_dependency_wait();  // the selection (and the zeroed counters)
   grid_dependents_launch();
-  const int T = a.q_len, G = a.groups, MB = a.max_blocks, Hg = a.heads_per_group, H = G * Hg;
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * kBmThreads + threadIdx.x;
-  if (e >= static_cast<int64_t>(a.batch) * T * G * kTopK) return;
-  const int s = static_cast<int>(e % kTopK);
-  const int64_t btg = e / kTopK;
-  const int g = static_cast<int>(btg % G), t = static_cast<int>((btg / G) % T), b = static_cast<int>(btg / (G * T));
-  const int L = a.seq_lens[b];
-  const bool ok = L > 0 && L >= T && L <= static_cast<int64_t>(MB) * kBlock;
-  const int n = bm_entry_block(a, b, g, t, s, L, ok);
-  if (n >= 0) {
-    atomicAdd(&w.cnt[(static_cast<int64_t>(b) * G + g) * MB + n], 1);
-  } else {
-    for (int h = 0; h < Hg; ++h)
-      w.pm[((static_cast<int64_t>(b) * T + t) * H + g * Hg + h) * kTopK + s] = make_float2(-INFINITY, 0.f);
+  if (static_cast<int>(blockIdx.x) >= count_ctas) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x - count_ctas) * kBmThreads + threadIdx.x;
+    const int64_t nq = static_cast<int64_t>(a.batch) * a.q_len * a.groups * a.heads_per_group * kDim / 16;
+    if (i >= nq) return;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q) + i);
+    const uint32_t wq[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      h[2 * k] = e4m3x2_to_f16x2(wq[k]);
+      h[2 * k + 1] = e4m3x2_to_f16x2(wq[k] >> 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(w.q16) + 2 * i;
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    return;
+  }
+  const int MB = a.max_blocks, Hg = a.heads_per_group, H = a.groups * Hg;
+  const bool use_hist = MB <= kPlanHistMax;
+  if (use_hist) {
+    for (int i = threadIdx.x; i < MB; i += kBmThreads) hist[i] = 0;
+    __syncthreads();
+  }
+  int bg, t0, n[kPlanPer];
+  plan_entries(a, blockIdx.x, bg, t0, n);
+  int32_t* cnt = w.cnt + static_cast<int64_t>(bg) * MB;
+  const int b = bg / a.groups, g = bg - b * a.groups;
+#pragma unroll
+  for (int k = 0; k < kPlanPer; ++k) {
+    const int e = threadIdx.x + k * kBmThreads, t = t0 + e / kTopK;
+    if (t >= a.q_len) continue;
+    if (n[k] >= 0) {
+      atomicAdd(use_hist ? &hist[n[k]] : &cnt[n[k]], 1);
+    } else {
+      for (int h = 0; h < Hg; ++h)
+        w.pm[((static_cast<int64_t>(b) * a.q_len + t) * H + g * Hg + h) * kTopK + e % kTopK] =
+            make_float2(-INFINITY, 0.f);
+    }
+  }
+  if (use_hist) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < MB; i += kBmThreads)
+      if (hist[i] > 0) atomicAdd(&cnt[i], hist[i]);
   }
 }
 
@@ -123,22 +187,37 @@ __global__ void __launch_bounds__(kPlanThreads) bm_scan_kernel(const AttnArgs a,
   if (tid == kPlanThreads - 1) off[MB] = base + incl;
 }
 
-// Plan, scatter: every valid entry (t * 16 + slot) to its block's list.
+// Plan, scatter: every valid entry (t * 16 + slot) to its block's list.  A chunk reserves one
+// run of each block's list with one atomic on the block's cursor (its count from the
+// shared-memory histogram) and hands the places inside the run out with shared atomics.
 __global__ void __launch_bounds__(kBmThreads) bm_scatter_kernel(const AttnArgs a, BmWorkspace w) {
+  extern __shared__ int32_t hist[];  // [max_blocks] when max_blocks <= kPlanHistMax
   grid_dependency_wait();
   grid_dependents_launch();
-  const int T = a.q_len, G = a.groups, MB = a.max_blocks;
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * kBmThreads + threadIdx.x;
-  if (e >= static_cast<int64_t>(a.batch) * T * G * kTopK) return;
-  const int s = static_cast<int>(e % kTopK);
-  const int64_t btg = e / kTopK;
-  const int g = static_cast<int>(btg % G), t = static_cast<int>((btg / G) % T), b = static_cast<int>(btg / (G * T));
-  const int L = a.seq_lens[b];
-  const bool ok = L > 0 && L >= T && L <= static_cast<int64_t>(MB) * kBlock;
-  const int n = bm_entry_block(a, b, g, t, s, L, ok);
-  if (n >= 0) {
-    const int64_t bgi = static_cast<int64_t>(b) * G + g;
-    w.ent[bgi * T * kTopK + atomicAdd(&w.cur[bgi * MB + n], 1)] = t * kTopK + s;
+  const int MB = a.max_blocks;
+  const bool use_hist = MB <= kPlanHistMax;
+  if (use_hist) {
+    for (int i = threadIdx.x; i < MB; i += kBmThreads) hist[i] = 0;
+    __syncthreads();
+  }
+  int bg, t0, n[kPlanPer];
+  plan_entries(a, blockIdx.x, bg, t0, n);
+  int32_t* cur = w.cur + static_cast<int64_t>(bg) * MB;
+  int32_t* ent = w.ent + static_cast<int64_t>(bg) * a.q_len * kTopK;
+  if (use_hist) {
+#pragma unroll
+    for (int k = 0; k < kPlanPer; ++k)
+      if (n[k] >= 0) atomicAdd(&hist[n[k]], 1);
+    __syncthreads();
+    for (int i = threadIdx.x; i < MB; i += kBmThreads)
+      if (hist[i] > 0) hist[i] = atomicAdd(&cur[i], hist[i]);  // the run's first place
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < kPlanPer; ++k) {
+    if (n[k] < 0) continue;
+    const int e = threadIdx.x + k * kBmThreads;
+    ent[atomicAdd(use_hist ? &hist[n[k]] : &cur[n[k]], 1)] = (t0 + e / kTopK) * kTopK + e % kTopK;
   }
 }
 
@@ -235,27 +314,6 @@ __device__ __forceinline__ void tc_dequant_vt(const uint8_t* src, uint8_t* vdst,
                      __byte_perm(x[4][i], x[5][i], 0x7632), __byte_perm(x[6][i], x[7][i], 0x7632));
     }
   }
-}
-
-// FP8 E4M3 queries -> f16 (exact), 16 values per thread: the block attention gathers query
-// rows from this copy with asynchronous 16-byte copies straight into its swizzled tiles.
-__global__ void __launch_bounds__(kBmThreads) bm_q16_kernel(const AttnArgs a, BmWorkspace w) {
-  grid_dependency_wait();
-  grid_dependents_launch();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * kBmThreads + threadIdx.x;
-  const int64_t n = static_cast<int64_t>(a.batch) * a.q_len * a.groups * a.heads_per_group * kDim / 16;
-  if (i >= n) return;
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q) + i);
-  const uint32_t wq[4] = {v.x, v.y, v.z, v.w};
-  uint32_t h[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    h[2 * k] = e4m3x2_to_f16x2(wq[k]);
-    h[2 * k + 1] = e4m3x2_to_f16x2(wq[k] >> 16);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(w.q16) + 2 * i;
-  dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-  dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -711,31 +769,28 @@ cudaError_t launch_block_major_attention(const AttnArgs& a, const BmWorkspace& w
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // 1. plan: zero the counters, count, scan, scatter
-  const int64_t entries = static_cast<int64_t>(a.batch) * a.q_len * a.groups * kTopK;
-  const unsigned egrid = static_cast<unsigned>((entries + kBmThreads - 1) / kBmThreads);
+  // 1. plan: zero the counters, count (with the queries widened to f16 beside it), scan, scatter
+  const int64_t plan_ctas = static_cast<int64_t>(a.batch) * a.groups * ((a.q_len + kPlanTokens - 1) / kPlanTokens);
+  const int64_t q16n = static_cast<int64_t>(a.batch) * a.q_len * a.groups * a.heads_per_group * kDim / 16;
+  const size_t hist_bytes = a.max_blocks <= kPlanHistMax ? static_cast<size_t>(a.max_blocks) * sizeof(int32_t) : 0;
   cudaError_t e = cudaMemsetAsync(w.cnt, 0, static_cast<size_t>(a.batch) * a.groups * a.max_blocks * sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(egrid);
+  cfg.gridDim = dim3(static_cast<unsigned>(plan_ctas + (q16n + kBmThreads - 1) / kBmThreads));
   cfg.blockDim = dim3(kBmThreads);
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, bm_count_kernel, a, w);
+  cfg.dynamicSmemBytes = hist_bytes;
+  e = cudaLaunchKernelEx(&cfg, bm_count_kernel, a, w, static_cast<int>(plan_ctas));
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(static_cast<unsigned>(a.batch * a.groups));
   cfg.blockDim = dim3(kPlanThreads);
+  cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, bm_scan_kernel, a, w);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(egrid);
+  cfg.gridDim = dim3(static_cast<unsigned>(plan_ctas));
   cfg.blockDim = dim3(kBmThreads);
+  cfg.dynamicSmemBytes = hist_bytes;
   e = cudaLaunchKernelEx(&cfg, bm_scatter_kernel, a, w);
   if (e != cudaSuccess) return e;
-  // 2. the queries in f16, then the block-major attention
-  const int64_t q16n = static_cast<int64_t>(a.batch) * a.q_len * a.groups * a.heads_per_group * kDim / 16;
-  cfg.gridDim = dim3(static_cast<unsigned>((q16n + kBmThreads - 1) / kBmThreads));
-  cfg.blockDim = dim3(kBmThreads);
-  e = cudaLaunchKernelEx(&cfg, bm_q16_kernel, a, w);
-  if (e != cudaSuccess) return e;
-  // one CTA per SM, striding over the (sequence, group, block) units
+  // 2. the block-major attention, one CTA per SM, striding over the (sequence, group, block) units
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(bm_attn_kernel), kTcSmem);
   if (e != cudaSuccess) return e;
   const int64_t grid = units < num_sms ? units : num_sms;

@@ -218,3 +218,34 @@ def test_block_major_attention_repeatable_and_matches_team_kernel(case):
     err = np.abs(bf16_to_np(outs[0][0]) - bf16_to_np(team))
     assert err.max() <= 2e-2 and err.mean() <= 2e-3
     assert np.allclose(to_np(outs[0][1]), to_np(team_lse), rtol=1e-4, atol=1e-4)
+
+
+def test_block_major_plan_wide_table():
+    """The block-major plan counts each 128-token chunk's blocks in a shared-memory histogram
+    when a row has at most 12,288 blocks and with global atomics beyond: the same sequences
+    with the block table padded to 12,289 columns (-1 past each sequence) take the second
+    form and must give bit-identical outputs, both matching the oracle."""
+    need_gpu()
+    import torch
+    import block_sparse_attention_indexer_gb300 as msa
+    w, dw, cache, table, lens, q, qi = _setup("prefill_hg4_t80", [80, 3000 + 1], 80, 4, True)
+    ref_scores = OM.block_scores(qi, cache[4], cache[5], table, lens)
+    sel_np = OM.select_blocks(ref_scores, lens)
+    out_ref, lse_ref = OM.sparse_attention(q, *cache[:4], table, lens, sel_np, w.heads_per_group)
+    sel = torch.from_numpy(sel_np).cuda()
+    B, T, H = w.batch, w.q_len, w.num_heads
+    wide = torch.full((B, 12289), -1, dtype=torch.int32, device="cuda")
+    wide[:, :table.shape[1]] = dw.batch.block_table
+    batches = [dw.batch, msa.Batch(wide, dw.batch.seq_lens, T)]
+    res = []
+    for batch in batches:
+        out = torch.zeros(B, T, H, 128, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros(B, T, H, dtype=torch.float32, device="cuda")
+        ws = msa.alloc_workspace(msa.MSA_OP_SPARSE_ATTN, dw.cfg, batch)
+        msa.msa_sparse_attn_decode(dw.cfg, dw.cache, batch, dw.q, sel, out, lse, ws)
+        torch.cuda.synchronize()
+        assert msa.msa_read_device_error(ws) == 0
+        assert_out_close(bf16_to_np(out), out_ref)
+        assert np.allclose(to_np(lse), lse_ref, rtol=1e-4, atol=1e-4)
+        res.append((out, lse))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
