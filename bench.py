@@ -71,14 +71,15 @@ def indexer_kernel_for(q_len: int, groups: int) -> str:
 def decode_path(batch: int, q_len: int, groups: int, max_blocks: int):
     """The attention form msa_decode takes and the kernels it launches per step.
 
-    From 64 query tokens on: the block-major attention (CSR count, scan and scatter, f16
-    queries, tcgen05 block attention, log-sum-exp merge) after the indexer and the selection.
+    From 64 query tokens on: the block-major attention (CSR count with the f16 queries beside
+    it, scan and scatter, tcgen05 block attention, log-sum-exp merge) after the indexer and the
+    selection.
     A small batch (at most 128 token x group rows of at most 256 blocks): the indexer, the
     attention whose producers select their rows, and the merge.  Otherwise the indexer, the
     selection, the team attention and its merge.
     """
     if q_len >= 64:
-        return "block-major (K-to-Q CSR, tcgen05)", 8
+        return "block-major (K-to-Q CSR, tcgen05)", 7
     if batch * q_len * groups <= 128 and max_blocks <= 256:
         return "query-major teams (mma.sync), selection in the attention's producers", 3
     return "query-major teams (mma.sync)", 4

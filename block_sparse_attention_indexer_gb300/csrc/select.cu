@@ -265,11 +265,13 @@ cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
   // are read from L2 on each pass
   a.row_cap = a.max_blocks < 4096 ? a.max_blocks : 4096;
   const size_t smem = static_cast<size_t>(kSelWarps) * a.row_cap * sizeof(uint32_t);
-  // rows of up to 768 candidates (e.g. chunked prefill on a 96K context) keep 24 candidates
-  // per lane in registers instead of 32: fewer registers, more rows in flight per SM
-  const bool short_rows = a.max_blocks <= 32 * 24;
-  const void* kern = short_rows ? reinterpret_cast<const void*>(select_kernel<24>)
-                                : reinterpret_cast<const void*>(select_kernel<32>);
+  // shorter rows keep fewer candidates per lane in registers (24 up to 768 candidates, e.g.
+  // chunked prefill on a 96K context; 18 up to 576, a 72K context): fewer registers and
+  // instructions per row, more rows in flight per SM
+  const int kpl = a.max_blocks <= 32 * 18 ? 18 : (a.max_blocks <= 32 * 24 ? 24 : 32);
+  const void* kern = kpl == 18 ? reinterpret_cast<const void*>(select_kernel<18>)
+                               : (kpl == 24 ? reinterpret_cast<const void*>(select_kernel<24>)
+                                            : reinterpret_cast<const void*>(select_kernel<32>));
   cudaError_t e = ensure_dynamic_smem(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -282,7 +284,9 @@ cudaError_t launch_select(const SelectArgs& a0, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = short_rows ? cudaLaunchKernelEx(&cfg, select_kernel<24>, a) : cudaLaunchKernelEx(&cfg, select_kernel<32>, a);
+  e = kpl == 18   ? cudaLaunchKernelEx(&cfg, select_kernel<18>, a)
+      : kpl == 24 ? cudaLaunchKernelEx(&cfg, select_kernel<24>, a)
+                  : cudaLaunchKernelEx(&cfg, select_kernel<32>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -139,6 +139,53 @@ def test_select_overflow_fallback():
     assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("MB", [576, 768, 1024])
+def test_select_warp_per_row_edges(MB):
+    """More than 2,048 rows of at most 1,024 candidates take the warp-per-row kernel, whose
+    instance holds 18, 24 or 32 candidates per lane by the row length: heavy ties, NaN and
+    -inf, signed zeros, rows whose survivors of the first filter exceed 32 (the arg-max
+    rounds) or the buffer (all scores equal: the full-row rounds), and every recent-block
+    position class; 1,050 sequences x 2 KV groups, each row compared with the oracle's."""
+    need_gpu()
+    import torch
+    import block_sparse_attention_indexer_gb300 as msa
+    rng = np.random.default_rng(MB)
+    B, G = 1050, 2
+    scores = np.zeros((B, 1, G, MB), dtype=np.float32)
+    for i in range(B * G):
+        kind = i % 6
+        if kind == 0:
+            s = rng.integers(-3, 4, size=MB).astype(np.float32)
+        elif kind == 1:
+            s = rng.standard_normal(MB).astype(np.float32)
+            s[rng.random(MB) < 0.3] = np.nan
+            s[rng.random(MB) < 0.3] = -np.inf
+        elif kind == 2:
+            lane = np.arange(MB) % 32
+            s = np.where(lane < 15, 1000.0 - 10 * lane + np.arange(MB) / 8192.0, -np.arange(MB, dtype=np.float64))
+            s = s.astype(np.float32)
+        elif kind == 3:
+            s = np.zeros(MB, dtype=np.float32)
+            s[rng.random(MB) < 0.5] = -0.0
+        else:
+            s = rng.standard_normal(MB).astype(np.float32)
+        scores[i // G, 0, i % G] = s
+    r = np.array([[0, 15, 16, 31, MB - 1][b % 5] if b % 6 else int(rng.integers(0, MB)) for b in range(B)])
+    pos = r * 128 + rng.integers(0, 128, size=B)
+    lens = (pos + 1).astype(np.int32)
+    table = np.zeros((B, MB), dtype=np.int32)
+    batch = msa.Batch(torch.from_numpy(table).cuda(), torch.from_numpy(lens).cuda(), 1)
+    cfg = msa.Config(num_kv_groups=G, heads_per_group=1)
+    sel = torch.full((B, 1, G, 16), 99, dtype=torch.int32, device="cuda")
+    msa.msa_select_blocks(cfg, batch, torch.from_numpy(scores).cuda(), sel)
+    torch.cuda.synchronize()
+    got = to_np(sel)
+    for b in range(B):
+        for g in range(G):
+            want = OM.select_row(scores[b, 0, g].astype(np.float64), int(pos[b]))
+            assert np.array_equal(got[b, 0, g], want), (b, g)
+
+
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_attention_on_oracle_selection(case):
     need_gpu()
