@@ -71,3 +71,26 @@ def test_cpu_sample_tracks_the_mean_context():
     assert abs(np.mean(lens[picks]) / np.mean(lens) - 1) < 0.05
     assert bench.representative_sequences(lens, 100) == sorted(range(len(lens)))
     assert bench.representative_sequences(np.array([5, 1, 3]), 1) == [2]
+
+
+def test_decode_path_matches_the_library_dispatch():
+    """bench.py's launch count per step follows msa_decode's own choice: block-major from
+    kBlockMajorMinTokens query tokens, the attention selecting its own rows for at most
+    kFusedSelectMaxRows rows of at most kFusedSelectMaxBlocks blocks, else the selection
+    kernel; the thresholds are read from the library's sources."""
+    consts = "".join(open(os.path.join(CSRC, f)).read() for f in os.listdir(CSRC) if f.endswith((".h", ".cuh", ".cu")))
+    bm_min = int(re.search(r"kBlockMajorMinTokens\s*=\s*(\d+)", consts).group(1))
+    max_rows = int(re.search(r"kFusedSelectMaxRows\s*=\s*(\d+)", consts).group(1))
+    max_blocks = int(re.search(r"kFusedSelectMaxBlocks\s*=\s*(\d+)", consts).group(1))
+    api = open(os.path.join(CSRC, "api.cu")).read()
+    assert "rows_tg(batch, cfg) <= kFusedSelectMaxRows" in api and "batch->max_blocks <= kFusedSelectMaxBlocks" in api
+    for batch in (1, 8, 32, 33, 64):
+        for q_len in (1, 2, 8, 63, 64, 100):
+            for mb in (32, max_blocks, max_blocks + 1, 1024):
+                form, n = bench.decode_path(batch, q_len, 4, mb)
+                if q_len >= bm_min:
+                    assert n == 7 and form.startswith("block-major")
+                elif batch * q_len * 4 <= max_rows and mb <= max_blocks:
+                    assert n == 3
+                else:
+                    assert n == 4
